@@ -24,6 +24,7 @@ decode (batch 128 x 32768 tokens) full, with a 128-token window, and the two alt
 path) on bounded samples of the same workload on the host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       python bench.py --profile CASE [--reps R]   (small driver for ncu captures)
 With N > 1 (torchrun) every rank runs an independent replica (the op has no
 exchange step); value = units of all ranks / max-over-ranks time.
 """
@@ -302,6 +303,11 @@ def run_ours(args):
     qq, qk, qv = qp.q.to(dev), qp.k.to(dev), qp.v.to(dev)
     qs, qcu = qp.sinks.to(dev), qp.cu_seqlens.to(dev)
     qout = torch.empty_like(qq)
+    # the same tensors with sinks -inf (standard softmax attention): the q, k and v draws
+    # come before the sinks, so both sink settings share them
+    qp_ninf = wl.qwen_prefill(seed=0, sinks="-inf")
+    assert torch.equal(qp_ninf.q, qp.q) and torch.equal(qp_ninf.k, qp.k)
+    qs_ninf = qp_ninf.sinks.to(dev)
     qd = wl.qwen_decode(seed=0)
     qdq, qdk, qdv = qd.q.to(dev), qd.k_cache.to(dev), qd.v_cache.to(dev)
     qdpt, qdsl, qdsk = qd.page_table.to(dev), qd.seq_lens.to(dev), qd.sinks.to(dev)
@@ -312,6 +318,10 @@ def run_ours(args):
 
     def q_prefill():
         sa.sink_attn_prefill(qq, qk, qv, qs, qcu, qp.max_seqlen, window=0, scale=qp.scale,
+                             out=qout, stream=stream)
+
+    def q_prefill_ninf():
+        sa.sink_attn_prefill(qq, qk, qv, qs_ninf, qcu, qp.max_seqlen, window=0, scale=qp.scale,
                              out=qout, stream=stream)
 
     def q_decode():
@@ -335,6 +345,7 @@ def run_ours(args):
         return sum(ts) / len(ts)
 
     q_prefill_ms = timed_mean(q_prefill, max(args.steps, 3))
+    q_prefill_ninf_ms = timed_mean(q_prefill_ninf, max(args.steps, 3))
     q_decode_ms = timed_mean(q_decode, max(args.steps, 3))
     qfkc, qfks = sa.sink_attn_quantize_fp8(qdk)
     qfvc, qfvs = sa.sink_attn_quantize_fp8(qdv)
@@ -490,6 +501,12 @@ def run_ours(args):
                          "frac": round(prefill_flops(qp) / (q_prefill_ms * 1e-3) / 1e12 / peak_tc, 4),
                          "ms": round(q_prefill_ms, 4), "workload": qp.name,
                          "note": "measured beside the step (not part of it)"},
+        "prefill_qwen_sinks_ninf": {
+            "value": round(prefill_flops(qp_ninf) / (q_prefill_ninf_ms * 1e-3) / 1e12, 3),
+            "unit": "TFLOP/s",
+            "frac": round(prefill_flops(qp_ninf) / (q_prefill_ninf_ms * 1e-3) / 1e12 / peak_tc, 4),
+            "ms": round(q_prefill_ninf_ms, 4), "workload": qp_ninf.name,
+            "note": "measured beside the step (not part of it)"},
         "decode_qwen": {"value": round(decode_bytes(qd) / (q_decode_ms * 1e-3) / 1e9, 2),
                         "unit": "GB/s",
                         "frac": round(decode_bytes(qd) / (q_decode_ms * 1e-3) / 1e9 / peak_hbm, 4),
@@ -544,6 +561,7 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(pc, args.cpu_seconds)
+        result["cpu_baseline"]["decode"] = cpu_baseline_decode(dc)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws > 1:
@@ -576,6 +594,22 @@ def cpu_baseline(pc, seconds):
                       f"{t_total:.1f} s"}
 
 
+def cpu_baseline_decode(dc):
+    """The fp64 oracle on the whole gpt-oss decode (every output), timed once on all host
+    cores; reported in the decode's own unit (algorithmic bytes per second)."""
+    import oracle
+    from gqa_attention_head_gb300 import workloads as wl
+    args = (wl.bf16_bits(dc.q), wl.bf16_bits(dc.k_cache), wl.bf16_bits(dc.v_cache),
+            dc.page_table.numpy(), dc.seq_lens.numpy(), dc.sinks.numpy())
+    oracle.decode(*args, window=dc.window, scale=dc.scale)  # untimed: loads and warms up
+    t0 = time.perf_counter()
+    oracle.decode(*args, window=dc.window, scale=dc.scale)
+    dt = time.perf_counter() - t0
+    return {"value": round(decode_bytes(dc) / dt / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle", "seconds": round(dt, 4),
+            "sample": f"every output of the {dc.name} ({dc.batch} sequences), once"}
+
+
 def step_config(pc, decode_name, decode_batch, decode_tokens, extra):
     """The `config` of both arms' JSON lines: the timed step's workloads and their sizes."""
     cfg = {"workload": pc.name + " | same with window 128 | " + decode_name,
@@ -586,7 +620,13 @@ def step_config(pc, decode_name, decode_batch, decode_tokens, extra):
 
 
 def run_reference(args):
-    """The reference arm: the fp64 CPU oracle on bounded samples of the same workload."""
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores. Each step
+    runs the step's three workloads, the causal prefill on a bounded sample of random
+    (token, head) rows (its whole would take about 20 s) and the windowed prefill and the
+    decode whole; `value` is the causal prefill's rate on its sample (the same metric and
+    unit as the GPU arm's headline), `ms_per_step` the measured wall time of one such
+    step, and `extrapolated_full_step_ms` the time the whole step would take at the
+    measured rates."""
     ws, rank, local = dist_env()
     if rank != 0:
         return
@@ -594,32 +634,143 @@ def run_reference(args):
     import oracle
     oracle.build.build()
     pc = wl.gptoss_prefill(seed=0, window=0)
-    # the decode's lengths are the first draw of its seeded generator: no cache needed here
-    dlen = wl.gptoss_decode_lengths(torch.Generator().manual_seed(0))
-    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    pw = wl.gptoss_prefill(seed=0, window=128)
+    dc = wl.gptoss_decode(seed=0)
+    qb, kb, vb = wl.bf16_bits(pc.q), wl.bf16_bits(pc.k), wl.bf16_bits(pc.v)
+    dargs = (wl.bf16_bits(dc.q), wl.bf16_bits(dc.k_cache), wl.bf16_bits(dc.v_cache),
+             dc.page_table.numpy(), dc.seq_lens.numpy(), dc.sinks.numpy())
+    # seconds of causal-prefill rows per step, so that the whole run stays within minutes
+    per_step = max(1.0, min(8.0, 100.0 / max(1, args.steps + args.warmup)))
+
+    def step():
+        t0 = time.perf_counter()
+        cb = cpu_baseline(pc, per_step)
+        t1 = time.perf_counter()
+        oracle.prefill(qb, kb, vb, pw.sinks.numpy(), pw.cu_seqlens.numpy(), window=pw.window,
+                       scale=pw.scale)
+        t2 = time.perf_counter()
+        oracle.decode(*dargs, window=dc.window, scale=dc.scale)
+        t3 = time.perf_counter()
+        return cb, (t3 - t0) * 1e3, (t2 - t1) * 1e3, (t3 - t2) * 1e3
+
     for _ in range(args.warmup):
-        cpu_baseline(pc, per_step)
-    vals = [cpu_baseline(pc, per_step) for _ in range(args.steps)]
-    value = sum(v["value"] for v in vals) / len(vals)
-    flops_per_step = prefill_flops(pc)
-    ms_per_step = flops_per_step / (value * 1e12) * 1e3
+        step()
+    runs = [step() for _ in range(args.steps)]
+    value = sum(r[0]["value"] for r in runs) / len(runs)
+    ms_per_step = sum(r[1] for r in runs) / len(runs)
+    w_ms = sum(r[2] for r in runs) / len(runs)
+    d_ms = sum(r[3] for r in runs) / len(runs)
+    full_causal_ms = prefill_flops(pc) / (value * 1e12) * 1e3
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16 inputs of the gpt-oss attention shapes)",
-        "config": step_config(pc, wl.GPTOSS_DECODE_NAME, len(dlen), sum(dlen), {
+        "config": step_config(pc, dc.name, dc.batch, dc.visible_tokens(), {
             "parallelism": "host cores (OpenMP)",
-            "timed": "the causal prefill (the headline value), on sampled rows",
+            "timed": "per step: the causal prefill on sampled rows (the headline value), the "
+                     "window-128 prefill and the decode whole",
         }),
         "impl": "reference",
+        "extrapolated_full_step_ms": round(full_causal_ms + w_ms + d_ms, 1),
+        "part_ms": {"prefill_causal_sampled": round(ms_per_step - w_ms - d_ms, 1),
+                    "prefill_w128": round(w_ms, 1), "decode": round(d_ms, 1)},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
-                         "cores": vals[0]["cores"],
-                         "sample": f"each step: random (token, head) rows for ~{per_step:.0f} s"},
+                         "cores": runs[0][0]["cores"],
+                         "sample": f"each step: random (token, head) rows of the causal "
+                                   f"prefill for ~{per_step:.0f} s, then the window-128 "
+                                   f"prefill and the decode whole"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+PROFILE_CASES = ("prefill_gptoss", "prefill_gptoss_w128", "prefill_qwen", "prefill_qwen_ninf",
+                 "prefill_paged", "decode_gptoss", "decode_gptoss_fp8", "decode_qwen",
+                 "decode_qwen_fp8")
+
+
+def run_profile(args):
+    """A small driver for ncu captures: one workload's inputs on the device and nothing else
+    (no L2 flush buffers, no other workload), the kernel launched `--reps` times. Prints
+    one line with the last launch's time; that time is not a bench value."""
+    import gqa_attention_head_gb300 as sa
+    from gqa_attention_head_gb300 import _build
+    from gqa_attention_head_gb300 import workloads as wl
+    _build.build()
+    sa.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    name = args.profile
+    if name.startswith("prefill") and name != "prefill_paged":
+        pc = {"prefill_gptoss": lambda: wl.gptoss_prefill(0, window=0),
+              "prefill_gptoss_w128": lambda: wl.gptoss_prefill(0, window=128),
+              "prefill_qwen": lambda: wl.qwen_prefill(0, sinks="normal"),
+              "prefill_qwen_ninf": lambda: wl.qwen_prefill(0, sinks="-inf")}[name]()
+        q, k, v = pc.q.to(dev), pc.k.to(dev), pc.v.to(dev)
+        sk, cu = pc.sinks.to(dev), pc.cu_seqlens.to(dev)
+        out = torch.empty_like(q)
+        work, unit = prefill_flops(pc), "flop"
+
+        def fn():
+            sa.sink_attn_prefill(q, k, v, sk, cu, pc.max_seqlen, window=pc.window,
+                                 scale=pc.scale, out=out, stream=stream)
+    elif name == "prefill_paged":
+        cp = wl.gptoss_chunked_prefill(seed=0)
+        cq, ckn, cvn = cp.q.to(dev), cp.k_new.to(dev), cp.v_new.to(dev)
+        ckc, cvc = cp.k_cache.to(dev), cp.v_cache.to(dev)
+        cpt, ccu, csl, csk = (cp.page_table.to(dev), cp.cu_seqlens.to(dev),
+                              cp.seq_lens.to(dev), cp.sinks.to(dev))
+        out = torch.empty_like(cq)
+        work, unit = 4.0 * cp.q.shape[2] * cp.q.shape[1] * cp.visible_pairs(), "flop"
+
+        def fn():
+            sa.sink_attn_prefill_paged(cq, ckn, cvn, ckc, cvc, cpt, ccu, csl, csk, cp.max_q_len,
+                                       cp.max_seq_len, window=0, scale=cp.scale, out=out,
+                                       stream=stream)
+    else:
+        fp8 = name.endswith("_fp8")
+        if name.startswith("decode_qwen"):
+            dc = wl.qwen_decode(seed=0)
+        else:
+            dc = wl.gptoss_decode(seed=0)
+        dq, dk, dv = dc.q.to(dev), dc.k_cache.to(dev), dc.v_cache.to(dev)
+        dpt, dsl, dsk = dc.page_table.to(dev), dc.seq_lens.to(dev), dc.sinks.to(dev)
+        need = sa.sink_attn_decode_workspace_bytes(dc.batch, dc.num_q_heads, dc.head_dim,
+                                                   dc.max_seq_len, dc.kv_chunk)
+        ws_ = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(dq)
+        if fp8:
+            kc, ks = sa.sink_attn_quantize_fp8(dk)
+            vc, vs = sa.sink_attn_quantize_fp8(dv)
+            del dk, dv
+
+            def fn():
+                sa.sink_attn_decode_fp8(dq, kc, vc, ks, vs, dpt, dsl, dsk, dc.max_seq_len,
+                                        window=dc.window, scale=dc.scale, kv_chunk=dc.kv_chunk,
+                                        workspace=ws_, out=out, stream=stream)
+        else:
+            def fn():
+                sa.sink_attn_decode(dq, dk, dv, dpt, dsl, dsk, dc.max_seq_len, window=dc.window,
+                                    scale=dc.scale, kv_chunk=dc.kv_chunk, workspace=ws_, out=out,
+                                    stream=stream)
+        work, unit = decode_bytes(dc, fp8=fp8), "byte"
+    ms = 0.0
+    for _ in range(args.reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+    st, bits = sa.sink_attn_read_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {bits:#x}")
+    print(json.dumps({"profile": name, "reps": args.reps, "algorithmic": work, "unit": unit,
+                      "last_ms": round(ms, 4),
+                      "note": "small-driver run for ncu; not a bench value"}), flush=True)
 
 
 def main():
@@ -630,7 +781,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=PROFILE_CASES, default=None,
+                    help="small driver for ncu: only this workload's kernel, --reps launches")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -669,7 +669,10 @@ def sink_attn_decode_static_workspace(q, k_cache, v_cache, page_table, seq_lens,
     a fixed 16 MiB array inside the library; sizes that need more are rejected with
     SINK_ATTN_ERR_WORKSPACE. Calls that overlap on the GPU share that array and race:
     serialise them. Arguments and results are those of ``sink_attn_decode``; pass
-    ``out`` to keep the call itself free of torch allocations too.
+    ``out`` to keep the call itself free of torch allocations too. The first call on a
+    device looks up the array there; with CUDA's default lazy module loading that lookup
+    also loads the module and reserves the array (it may allocate and synchronise), so
+    make one warm-up call per device before a latency-critical loop or a stream capture.
     """
     dev = q.device
     if dev.type != "cuda":

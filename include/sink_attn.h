@@ -64,7 +64,9 @@
  * Conventions shared by every entry point
  *   - Every pointer is device memory owned by the caller (sink_attn_prefill_from_host
  *     also takes host arrays, named *_host). The library allocates and frees no memory;
- *     decode scratch is the caller's `workspace`.
+ *     decode scratch is the caller's `workspace`. The one exception is
+ *     sink_attn_decode_static_workspace, whose scratch is a fixed array inside the
+ *     library (reserved when its module is loaded on a device, see there).
  *   - Every call is asynchronous on `stream` and never synchronises the host.
  *     Host-side size arguments (max_seqlen, max_seq_len, total_tokens) exist so
  *     that no device array has to be read back.
@@ -192,9 +194,14 @@ sink_attn_status sink_attn_decode(const sink_attn_bf16* q, const sink_attn_bf16*
  * library, SINK_ATTN_STATIC_WORKSPACE_BYTES long, reserved on every GPU that loads
  * the library until the process exits. Sizes whose scratch
  * (sink_attn_decode_workspace_bytes with the window applied) exceeds it are rejected
- * with SINK_ATTN_ERR_WORKSPACE before anything is launched. The call allocates no
- * memory. The first call on a device looks up the array's device address there
- * (once per device, with that device current); make that first call before any
+ * with SINK_ATTN_ERR_WORKSPACE before anything is launched. The call itself allocates
+ * nothing. The first call on a device looks up the array's device address there
+ * (once per device, with that device current). CUDA loads a library's device code
+ * lazily by default (CUDA_MODULE_LOADING=LAZY): the module that holds the array is then
+ * loaded, and its memory reserved by the driver, during that first lookup, which may
+ * allocate and synchronise. So the array is held on every GPU where this entry point
+ * has been called (on every GPU that loads the library when loading is eager), and one
+ * warm-up call per device belongs before the latency-critical loop and before any
  * stream capture. Every call shares the one array and leaves its contents behind;
  * nothing in it needs to start at zero, but calls that overlap on the GPU (other
  * streams, other threads) race on it: serialise them.

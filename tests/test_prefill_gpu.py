@@ -178,8 +178,10 @@ def test_prefill_host_validation():
 
 
 # ---------------------------------------------------------------------------
-# Full-size workloads: the GPU output in full, the oracle on sampled rows
-# (first/last rows of every sequence, tile boundaries, and random rows).
+# Full-size workloads. The four named prefill workloads are compared with the oracle on
+# every output element (the oracle takes tens of seconds per workload on the host cores);
+# the two 32768-token sequences, too long for that, on sampled rows (first/last rows of
+# every sequence, tile boundaries, and random rows) plus a property that holds everywhere.
 # ---------------------------------------------------------------------------
 
 def sample_rows(case, n_random, seed):
@@ -208,6 +210,23 @@ FULL = {
     "gpt-oss prefill W128": lambda: wl.gptoss_prefill(0, window=128),
     "Qwen3-235B prefill sinks -inf": lambda: wl.qwen_prefill(0, sinks="-inf"),
     "Qwen3-235B prefill sinks N(0,1)": lambda: wl.qwen_prefill(0, sinks="normal"),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_prefill_full_size_every_element(name):
+    """Every (token, head, d) of a named full-size workload against the fp64 oracle, at the
+    strict bound over the whole tensor: the late units of the snake schedule, the deferred
+    epilogues across unit boundaries and the rescales of long rows are all covered."""
+    case = FULL[name]()
+    got = gpu_prefill(case)
+    torch.cuda.synchronize()
+    assert_clean_device()
+    ref = ref_prefill(case)
+    assert_parity(got, ref, name, strict=True)
+
+
+LONG = {
     # the longest single sequences: 256 q tiles x 256 key tiles in one causal unit chain
     "one 32768-token sequence D64 G8 causal": lambda: wl.prefill_case([32768], 64, 8, 64,
                                                                       seed=77),
@@ -216,9 +235,9 @@ FULL = {
 }
 
 
-@pytest.mark.parametrize("name", list(FULL))
-def test_prefill_full_size_sampled(name):
-    case = FULL[name]()
+@pytest.mark.parametrize("name", list(LONG))
+def test_prefill_long_sequence_sampled(name):
+    case = LONG[name]()
     got = gpu_prefill(case)
     torch.cuda.synchronize()
     assert torch.isfinite(got.float()).all()
@@ -233,7 +252,6 @@ def test_prefill_full_size_sampled(name):
     vmax = case.v.float().abs().max().item()
     assert got.float().abs().max().item() <= vmax * (1 + 1e-2)
     assert_clean_device()
-
 
 
 @pytest.mark.parametrize("d", [64, 128])

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import gqa_attention_head_gb300 as sa
+import oracle
 from gqa_attention_head_gb300 import _build
 from gqa_attention_head_gb300 import workloads as wl
 from parity import assert_parity
@@ -43,10 +44,12 @@ def call_static(lib, dc, q, kc, vc, pt, sl, sk, out, max_seq_len, kv_chunk, wind
         dc.scale, kv_chunk, ptr(out), stream)
 
 
-@pytest.mark.parametrize("window", [0, 300])
+@pytest.mark.parametrize("window", [0, 1500])
 def test_static_workspace_matches_caller_workspace_twice(lib, window):
-    # 16 sequences of up to 5000 positions with 512-token chunks: up to 10 chunks each,
-    # 16*64*10*65*4 bytes of scratch (2.7 MB), well inside the 16 MiB array.
+    # 16 sequences of up to 5000 positions with 512-token chunks: up to 10 chunks each
+    # (3 with the 1500-token window), 16*64*10*65*4 bytes of scratch (2.7 MB), well inside
+    # the 16 MiB array. Every case has sequences that span several chunks, so the partial
+    # results do pass through the array.
     dc = wl.decode_case([5000, 1, 17, 1024, 1025, 4096, 3000, 0, 2222, 4999, 512, 513, 77,
                          4000, 2500, 1500], 64, 8, 64, seed=31, kv_chunk=512)
     q, kc, vc = dc.q.cuda(), dc.k_cache.cuda(), dc.v_cache.cuda()
@@ -54,12 +57,17 @@ def test_static_workspace_matches_caller_workspace_twice(lib, window):
     ref = sa.sink_attn_decode(q, kc, vc, pt, sl, sk, dc.max_seq_len, window=window,
                               scale=dc.scale, kv_chunk=512)
     torch.cuda.synchronize()
+    exact = oracle.decode(wl.bf16_bits(dc.q), wl.bf16_bits(dc.k_cache), wl.bf16_bits(dc.v_cache),
+                          dc.page_table.numpy(), dc.seq_lens.numpy(), dc.sinks.numpy(),
+                          window=window, scale=dc.scale)
     for call in range(2):  # the second call reuses the array the first one left behind
         out = torch.full_like(q, float("nan"))
         st = call_static(lib, dc, q, kc, vc, pt, sl, sk, out, dc.max_seq_len, 512, window)
         assert st == 0, sa.sink_attn_status_string(st)
         torch.cuda.synchronize()
-        assert_parity(out, ref.double().cpu().numpy(), f"static scratch, call {call + 1}")
+        assert_parity(out, exact, f"static scratch vs oracle, call {call + 1}", strict=True)
+        assert_parity(out, ref.double().cpu().numpy(), f"static scratch vs caller scratch, "
+                      f"call {call + 1}", strict=True)
     st, bits = sa.sink_attn_read_device_error()
     assert st == 0, f"device error word {bits:#x}"
 
