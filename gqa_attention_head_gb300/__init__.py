@@ -658,6 +658,20 @@ def sink_attn_read_device_error(stream=None, device=None):
     return int(st), int(bits.value)
 
 
+def sink_attn_debug_decode_withhold_page(enable, wait_limit_ns=1_000_000_000):
+    """Test switch for the decode's failure path (process-wide; see include/sink_attn.h).
+
+    With ``enable``, later decode launches never copy the first page of (chunk 0, kv head 0,
+    sequence 0), so the wait for it runs out after ``wait_limit_ns`` and the device error
+    word gets SINK_ATTN_DEVERR_WAIT_TIMEOUT; ``enable=False`` restores normal launches.
+    """
+    lib = load_library()
+    fn = lib.sink_attn_debug_decode_withhold_page
+    fn.argtypes = [ctypes.c_int32, ctypes.c_uint64]
+    fn.restype = None
+    fn(1 if enable else 0, int(wait_limit_ns))
+
+
 def sink_attn_decode_static_workspace(q, k_cache, v_cache, page_table, seq_lens, sinks,
                                       max_seq_len, window=0, scale=None, kv_chunk=1024,
                                       out=None, stream=None):

@@ -57,7 +57,9 @@ struct DecodeParams {
   unsigned* err;
   int num_pages, max_pages, batch, max_seq_len, Hq, Hkv, G, window, chunk, cmax;
   float scale_log2;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;  // pipeline waits
+  uint64_t drain_ns;    // teardown waits for copies in flight
+  int withhold;         // test switch (see DecodeLaunch::withhold_first_page)
 };
 
 // Sequence length as used by both kernels: out-of-contract values are recorded
@@ -98,7 +100,8 @@ struct DecodeSmem {
   // depth that is a multiple of the consumer warps, the next use of a stage goes to the warp
   // that consumed its previous page, so no full-barrier wait is ever two phases ahead (where
   // the parity would match an already completed phase and the wait would pass early).
-  static_assert(kStages % kConsumerWarps == 0, "ring depth must be a multiple of the consumers");
+  static constexpr int kGroups = (NT == 2 && !F8) ? 2 : kConsumerWarps;  // page owners per round
+  static_assert(kStages % kGroups == 0, "ring depth must be a multiple of the consumer groups");
 };
 
 // Shared-memory byte address of 16-byte chunk `c` of token row `r` (0..15) in a page
@@ -124,6 +127,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
                                                   const DecodeParams& p) {
   using S = DecodeSmem<D, NT, F8, ST>;
   constexpr int kStages = S::kStages;
+  constexpr bool kSplitTiles = (NT == 2) && !F8;  // each consumer warp serves one head tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -151,7 +155,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kSplitTiles ? 2 : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -172,6 +176,9 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       int cur = lane < npg ? pt[lane] : -1;
       int nxt = 32 + lane < npg ? pt[32 + lane] : -1;
       int issued = 0;
+      // Test switch: page 0 of (chunk 0, kv head 0, sequence 0) is never copied, so the
+      // consumers' bounded wait for it runs out and the CTA aborts through its normal path.
+      const bool withheld = p.withhold && c == 0 && g == 0 && b == 0;
       for (int i = 0; i < npg; ++i) {
         if (i > 0 && (i & 31) == 0) {
           cur = nxt;
@@ -181,7 +188,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
         const int st = i % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * st, ((i / kStages) & 1) ^ 1, wc)))
           break;
-        if (elect_one()) {
+        if (elect_one() && !(withheld && i == 0)) {
           const uint32_t full = bar_full + 8 * st;
           if (pid < 0 || pid >= p.num_pages) {
             atomicOr(p.err, kErrPageId);
@@ -208,8 +215,10 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       }
       // Let every copy still in flight land before the CTA can exit.
       if (lane == 0) {
-        for (int i = max(0, issued - kStages); i < issued; ++i)
-          mbar_drain(bar_full + 8 * (i % kStages), (i / kStages) & 1, p.timeout_ns);
+        for (int i = max(0, issued - kStages); i < issued; ++i) {
+          if (withheld && i == 0) continue;  // no copy was issued for it
+          mbar_drain(bar_full + 8 * (i % kStages), (i / kStages) & 1, p.drain_ns);
+        }
       }
     }
     return;
@@ -218,22 +227,30 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
   // ---------------- consumers: warp w takes pages w, w+4, w+8, ... ----------------
   const int G = p.G;
   const int head0 = g * G;
+  // Two head tiles of a bf16 cache (a group of 16): warps 0-1 serve tile 0 and warps 2-3
+  // tile 1, each pair taking the even / odd pages, so a warp holds the Q fragments and
+  // running outputs of one tile only (92 registers instead of 128 with spills: four CTAs
+  // per SM instead of three). Otherwise every warp serves all tiles of its pages.
+  constexpr int NTW = kSplitTiles ? 1 : NT;  // head tiles per warp
+  const int tile0 = kSplitTiles ? (warp >> 1) : 0;
+  const int pfirst = kSplitTiles ? (warp & 1) : warp;
+  constexpr int pstep = kSplitTiles ? 2 : kConsumerWarps;
   // Q of the group as B fragments of S = K * Q^T (k = head_dim, n = query head).
   // bf16: lane (g, t) holds head_dim pairs 2t, 2t+1 and 2t+8, 2t+9 of each 16-wide slice.
   // FP8: f16, pairs 4t, 4t+1 and 4t+2, 4t+3 (the permuted k order of the K fragments),
   // scaled by 2^-qexp so that the group's largest |q| is below 2^15.
-  uint32_t qf[NT][D / 16][2];
+  uint32_t qf[NTW][D / 16][2];
   float qmul = 1.f;  // FP8: 2^qexp, applied to S in fp32
   if constexpr (F8) {
     auto q_quad = [&](int nt, int kk) {  // head_dim 16kk + 4t .. +3 of head nt*8 + g
-      const int hl = nt * 8 + (lane >> 2);
+      const int hl = (tile0 + nt) * 8 + (lane >> 2);
       if (hl >= G) return make_uint2(0u, 0u);
       const __nv_bfloat16* qrow = p.q + ((size_t)b * p.Hq + head0 + hl) * D;
       return *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * (lane & 3));
     };
     float qmax = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint2 raw = q_quad(nt, kk);
@@ -248,7 +265,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
     qmul = __int_as_float((127 + qexp) << 23);
     const float down = __int_as_float((127 - qexp) << 23);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint2 raw = q_quad(nt, kk);
@@ -259,8 +276,8 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       }
   } else {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int hl = nt * 8 + (lane >> 2);
+    for (int nt = 0; nt < NTW; ++nt) {
+      const int hl = (tile0 + nt) * 8 + (lane >> 2);
       const bool hv = hl < G;
       const uint32_t* qrow =
           reinterpret_cast<const uint32_t*>(p.q + ((size_t)b * p.Hq + head0 + (hv ? hl : 0)) * D);
@@ -271,10 +288,10 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       }
     }
   }
-  float m[NT][2], l[NT][2];
-  float o[NT][D / 16][4];
+  float m[NTW][2], l[NTW][2];
+  float o[NTW][D / 16][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NTW; ++nt) {
     m[nt][0] = m[nt][1] = -INFINITY;
     l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
@@ -283,7 +300,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
   const float sl = p.scale_log2 * qmul;
   bool aborted = false;
 
-  for (int i = warp; i < npg; i += kConsumerWarps) {
+  for (int i = pfirst; i < npg; i += pstep) {
     const int st = i % kStages;
     bool ok = mbar_wait(bar_full + 8 * st, (i / kStages) & 1, wc);
     ok = __all_sync(0xffffffffu, ok);
@@ -310,9 +327,9 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       __syncwarp();
     }
     // S[16 tokens x 8 heads] per head tile.
-    float s[NT][4];
+    float s[NTW][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < NTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
     const int mat = lane >> 3, rr = lane & 7;
     if constexpr (F8) {
 #pragma unroll
@@ -326,7 +343,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
           e4m3x4_to_f16x2x2(r[2 * hf], a[0], a[2]);      // token g: codes 4t, 4t+1 | 4t+2, 4t+3
           e4m3x4_to_f16x2x2(r[2 * hf + 1], a[1], a[3]);  // token g+8
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NTW; ++nt)
             mma_16816_f16(s[nt], a, qf[nt][2 * kc + hf][0], qf[nt][2 * kc + hf][1]);
         }
       }
@@ -336,7 +353,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
         uint32_t a[4];
         ldsm_x4(page_chunk_addr<D, false>(kbase, rr + ((mat & 1) << 3), 2 * kk + (mat >> 1)), a);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
+        for (int nt = 0; nt < NTW; ++nt) mma_16816(s[nt], a, qf[nt][kk][0], qf[nt][kk][1]);
       }
     }
     const int ta = tok0 + (lane >> 2), tb = ta + 8;
@@ -352,9 +369,9 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       pa = va ? sc[kPage + ra] * kPvScale : 0.f;
       pb_ = vb ? sc[kPage + ra + 8] * kPvScale : 0.f;
     }
-    uint32_t pb[NT][2];
+    uint32_t pb[NTW][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < NTW; ++nt) {
       const float x0 = va ? s[nt][0] * fa : -INFINITY;  // token a, head A
       const float x1 = va ? s[nt][1] * fa : -INFINITY;  // token a, head B
       const float x2 = vb ? s[nt][2] * fb : -INFINITY;  // token b, head A
@@ -405,7 +422,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
           e4m3x4_to_f16x2x2(sp, ae[x], ao[x]);
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NTW; ++nt) {
           mma_16816_f16(o[nt][2 * j], ae, pb[nt][0], pb[nt][1]);
           mma_16816_f16(o[nt][2 * j + 1], ao, pb[nt][0], pb[nt][1]);
         }
@@ -416,7 +433,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
         uint32_t a[4];
         ldsm_x4_trans(page_chunk_addr<D, false>(vbase, rr + ((mat >> 1) << 3), 2 * mt + (mat & 1)), a);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][mt], a, pb[nt][0], pb[nt][1]);
+        for (int nt = 0; nt < NTW; ++nt) mma_16816(o[nt][mt], a, pb[nt][0], pb[nt][1]);
       }
     }
     if (partial) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -427,14 +444,14 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
   // ---------------- combine the four warps (and the sink) ----------------
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");  // ring is free now
   if (*abort_flag) aborted = true;
-  constexpr int GP = NT * 8;  // padded heads per kv head
+  constexpr int GP = NTW * 8;  // heads held per warp (padded)
   static_assert(kConsumerWarps * GP * (2 + D) * 4 <= S::kRingBytes,
                 "the combine scratch must fit in the ring it reuses");
   float* cm = reinterpret_cast<float*>(smem);  // [4][GP]
   float* cl = cm + kConsumerWarps * GP;        // [4][GP]
   float* co = cl + kConsumerWarps * GP;        // [4][GP][D]
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
@@ -468,18 +485,22 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
   for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
     const int hl = idx / D, d = idx % D;
     const int h = head0 + hl;
+    // the warps holding head hl, and its index among their heads
+    constexpr int NW = kSplitTiles ? 2 : kConsumerWarps;
+    const int w0 = kSplitTiles ? 2 * (hl >> 3) : 0;
+    const int hh = kSplitTiles ? (hl & 7) : hl;
     const float sink_l2 = with_sink ? p.sinks[h] * kLog2e : -INFINITY;
     float M = sink_l2;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * GP + hl]);
+    for (int w = w0; w < w0 + NW; ++w) M = fmaxf(M, cm[w * GP + hh]);
     const float Mu = M == -INFINITY ? 0.f : M;
     float lsum = ex2(sink_l2 - Mu);
     float acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = ex2(cm[w * GP + hl] - Mu);
-      lsum += cl[w * GP + hl] * f;
-      acc += co[(w * GP + hl) * D + d] * f;
+    for (int w = w0; w < w0 + NW; ++w) {
+      const float f = ex2(cm[w * GP + hh] - Mu);
+      lsum += cl[w * GP + hh] * f;
+      acc += co[(w * GP + hh) * D + d] * f;
     }
     const float val = lsum > 0.f ? acc / lsum : 0.f;
     const size_t bh = (size_t)b * p.Hq + h;
@@ -500,11 +521,12 @@ __global__ void __launch_bounds__(kDecodeThreads)
   decode_split_body<D, NT, F8, ST>(tm_k, tm_v, p);
 }
 
-// Two head tiles at head_dim 128 (a group of 16 query heads), bf16 or FP8 cache:
-// registers, not shared memory, bound the resident CTAs; capping them for three CTAs per
-// SM gives the latency-bound consumers half as many warps again.
+// Two head tiles at head_dim 128 (a group of 16 query heads): registers, not shared memory,
+// bound the resident CTAs, and the latency-bound consumers gain from more of them. FP8
+// cache (every warp serves both tiles): capped for three CTAs per SM. bf16 cache (one tile
+// per warp, 92 registers): four CTAs per SM, Qwen3-235B-style decode 0.1471 -> 0.1409 ms.
 template <int D, int NT, bool F8, int ST>
-__global__ void __launch_bounds__(kDecodeThreads, 3)
+__global__ void __launch_bounds__(kDecodeThreads, F8 ? 3 : 4)
     decode_split_kernel_3(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   decode_split_body<D, NT, F8, ST>(tm_k, tm_v, p);
@@ -603,8 +625,9 @@ cudaError_t launch_split_ring(const DecodeLaunch& a, const DecodeParams& p, cuda
 // bf16: 8, except when no CTA reads more than 9 pages (a window of at most 128 tokens,
 // which may start inside a page): there every page fits a 4-page ring twice over, and the
 // smaller ring lets more CTAs stay resident, so a grid of short ranges runs in fewer
-// waves (long-context decode with a 128-token window: 17.2 -> 14.4 us). With two head
-// tiles the combine scratch needs the 8-page ring it reuses.
+// waves (long-context decode with a 128-token window: 17.2 -> 14.4 us). bf16 with two head
+// tiles: 6 pages (4, 6 and 8 measured within 1% of each other; each warp pair owns every
+// other page, so the depth must be even).
 template <int D, int NT, bool F8>
 cudaError_t launch_split(const DecodeLaunch& a, const DecodeParams& p, cudaStream_t stream) {
   if constexpr (F8) {
@@ -615,7 +638,8 @@ cudaError_t launch_split(const DecodeLaunch& a, const DecodeParams& p, cudaStrea
       const int pages = (min(vis, p.chunk) + kPage - 1) / kPage + 1;
       if (pages <= 9) return launch_split_ring<D, NT, F8, 4>(a, p, stream);
     }
-    return launch_split_ring<D, NT, F8, 8>(a, p, stream);
+    if constexpr (NT == 2) return launch_split_ring<D, NT, F8, 6>(a, p, stream);
+    else return launch_split_ring<D, NT, F8, 8>(a, p, stream);
   }
 }
 
@@ -646,6 +670,8 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
   p.cmax = a.cmax;
   p.scale_log2 = a.scale * kLog2e;
   p.timeout_ns = a.timeout_ns;
+  p.drain_ns = a.drain_ns;
+  p.withhold = a.withhold_first_page;
   const bool two_tiles = p.G > 8;
   if (a.fp8) {
     if (a.head_dim == 64)

@@ -44,7 +44,10 @@ struct DecodeLaunch {
   int num_pages, page_size, max_pages, batch, max_seq_len, num_q_heads, num_kv_heads, head_dim,
       window, kv_chunk, cmax;
   float scale;
-  uint64_t timeout_ns;
+  uint64_t timeout_ns;           // limit of every pipeline wait
+  uint64_t drain_ns;             // limit of the teardown waits for copies still in flight
+  int withhold_first_page;       // test switch: never copy page 0 of (chunk 0, kv head 0,
+                                 // sequence 0), so that its consumers' waits run out
 };
 
 // Number of split-KV chunks the grid provides for (window-limited visible range).

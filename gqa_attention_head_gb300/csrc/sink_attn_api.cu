@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -20,6 +21,11 @@ namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s per pipeline wait
 constexpr int kMaxDevices = 64;
+
+// Test switch of the decode launches (sink_attn_debug_decode_withhold_page): the first
+// page of (chunk 0, kv head 0, sequence 0) withheld, and the pipeline-wait limit.
+std::atomic<int> g_decode_withhold{0};
+std::atomic<uint64_t> g_decode_wait_ns{kWaitTimeoutNs};
 
 // Device error word: set by kernels (atomicOr of SINK_ATTN_DEVERR_* bits),
 // read and cleared by sink_attn_read_device_error.
@@ -150,6 +156,11 @@ const char* sink_attn_status_string(sink_attn_status s) {
     case SINK_ATTN_ERR_DEVICE: return "device-side check failed";
   }
   return "unknown status";
+}
+
+void sink_attn_debug_decode_withhold_page(int32_t enable, uint64_t wait_limit_ns) {
+  g_decode_wait_ns.store(enable ? wait_limit_ns : kWaitTimeoutNs);
+  g_decode_withhold.store(enable ? 1 : 0);
 }
 
 int32_t sink_attn_num_sms(void) { return num_sms_current(); }
@@ -311,7 +322,9 @@ sink_attn_status decode_impl(const sink_attn_bf16* q, const void* k_cache, const
   a.kv_chunk = kv_chunk;
   a.cmax = cmax;
   a.scale = scale;
-  a.timeout_ns = kWaitTimeoutNs;
+  a.timeout_ns = g_decode_wait_ns.load();
+  a.drain_ns = kWaitTimeoutNs;
+  a.withhold_first_page = g_decode_withhold.load();
   return sa::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SINK_ATTN_OK
              : SINK_ATTN_ERR_CUDA;

@@ -60,6 +60,7 @@
  *   sink_attn_quantize_fp8 / _append_kv_fp8 / _decode_fp8   the FP8 (e4m3) cache
  *   sink_attn_decode_workspace_bytes, sink_attn_status_string,
  *   sink_attn_read_device_error, sink_attn_num_sms
+ *   sink_attn_debug_decode_withhold_page   test switch for the decode's timeout path
  *
  * Conventions shared by every entry point
  *   - Every pointer is device memory owned by the caller (sink_attn_prefill_from_host
@@ -461,6 +462,19 @@ sink_attn_status sink_attn_read_device_error(sink_attn_stream_t stream, uint32_t
 /* Number of streaming multiprocessors the library sizes persistent grids for
  * on the current device (0 if no device is visible). Host query only. */
 int32_t sink_attn_num_sms(void);
+
+/*
+ * Test switch for the decode's failure path; the pages have no counterpart. With
+ * enable != 0, every later decode launch (sink_attn_decode, _decode_lse, _decode_fp8,
+ * _decode_static_workspace) never copies the first page of (chunk 0, kv head 0,
+ * sequence 0): the consumer warps' wait for it runs out after wait_limit_ns, the CTA
+ * sets SINK_ATTN_DEVERR_WAIT_TIMEOUT in the device error word, lets its copies in
+ * flight land (those waits keep their own 1 s limit), and returns without writing that
+ * sequence's partial results; every other CTA runs normally. Nothing traps and nothing
+ * waits without a limit. enable == 0 restores the normal launches (and the 1 s limit).
+ * The switch is process-wide, not per stream or thread: it exists for tests only.
+ */
+void sink_attn_debug_decode_withhold_page(int32_t enable, uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,9 @@ CASES = {
     "G16 D64 chunk128": dict(lens=LENS, hq=32, hkv=2, d=64, chunk=128),
     "G2 D128 W300": dict(lens=LENS, hq=4, hkv=2, d=128, chunk=128, window=300),
     "G16 D128 W100 chunk256": dict(lens=LENS, hq=32, hkv=2, d=128, chunk=256, window=100),
+    # groups between 8 and 16: the second head tile is partly padding
+    "G12 D128 chunk512": dict(lens=LENS, hq=24, hkv=2, d=128, chunk=512),
+    "G10 D64 chunk256": dict(lens=LENS, hq=20, hkv=2, d=64, chunk=256),
 }
 
 
@@ -259,3 +262,33 @@ def test_decode_graph_capture_matches_direct_call():
                         torch.clamp(dc.seq_lens - 999, min=1), dc.sinks, 0, dc.scale)
     assert_parity(out, ref_decode(dc2), "graph replay, shorter lengths", strict=True)
     assert_clean_device()
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(16, 2, 64), (64, 4, 128)])
+def test_decode_wait_timeout_reported_then_clean(hq, hkv, d):
+    """A pipeline wait that runs out: the test switch withholds the copy of one page (chunk 0,
+    kv head 0, sequence 0), so its consumers' bounded wait gives up after 20 ms. The call
+    returns, the device error word carries the timeout bit, every output outside the
+    aborted CTA's heads is still right, and the next normal call in the same process is
+    clean and matches the oracle."""
+    dc = wl.decode_case([3000, 1500, 17, 2100], hq, hkv, d, seed=41, kv_chunk=1024)
+    args = (dc.q.cuda(), dc.k_cache.cuda(), dc.v_cache.cuda(), dc.page_table.cuda(),
+            dc.seq_lens.cuda(), dc.sinks.cuda(), dc.max_seq_len)
+    ref = oracle.decode(bits(dc.q), bits(dc.k_cache), bits(dc.v_cache), dc.page_table.numpy(),
+                        dc.seq_lens.numpy(), dc.sinks.numpy(), window=0, scale=dc.scale)
+    sa.sink_attn_read_device_error()
+    sa.sink_attn_debug_decode_withhold_page(True, 20_000_000)
+    try:
+        out = sa.sink_attn_decode(*args, window=0, scale=dc.scale, kv_chunk=1024)
+        st, b = sa.sink_attn_read_device_error()
+    finally:
+        sa.sink_attn_debug_decode_withhold_page(False)
+    assert st == 5 and (b & 0x1), f"status {st}, bits {b:#x}"
+    G = hq // hkv
+    keep = torch.ones(dc.batch, hq, dtype=torch.bool)
+    keep[0, :G] = False  # the heads the aborted CTA serves
+    got = out.float().cpu()
+    assert_parity(got[keep], ref[keep.numpy()], "outside the aborted CTA", strict=True)
+    out = sa.sink_attn_decode(*args, window=0, scale=dc.scale, kv_chunk=1024)
+    assert_clean_device()
+    assert_parity(out, ref, "next call", strict=True)
