@@ -108,7 +108,14 @@ struct PrefillSmem {
   // Windowed head_dim 64: each softmax thread's pending epilogue (row, 1/d, log-sum-exp).
   static constexpr int kPend = (kPre + 2 * (kMaxSchedQTiles + 1) + 15) / 16 * 16;
   static constexpr int kPendBytes = (D == 64) ? 2 * 128 * 16 : 0;
-  static constexpr int kBytes = kPend + kPendBytes + 1024;  // + alignment slack
+  // head_dim 64: the CTA's units, decoded once at the start (48 bytes each; head_dim 128
+  // has no room left and decodes each unit when it starts). Window 128: 152 -> 129 us,
+  // causal 0.765 -> 0.743 ms: the lookup and the row-offset loads sat in every unit start.
+  // (Addressing the list through a 32-bit shared address moved the kernel's few spilled
+  // registers into the step loop and lost the gain: 0.764 ms.)
+  static constexpr int kMaxListUnits = (D == 64) ? 512 : 0;
+  static constexpr int kList = (kPend + kPendBytes + 15) / 16 * 16;
+  static constexpr int kBytes = kList + kMaxListUnits * 48 + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory per CTA");
 };
 
@@ -192,35 +199,56 @@ struct UnitSched {
   const uint16_t* pre;   // pre[qi] = sequence-units of q-tile indices < qi
   int total;             // valid units (snake) or all unit ids (round-robin)
   int snake;
+  const int4* list;      // LIST: the CTA's units decoded in shared memory (3 int4 each)
+  int n_list;
 };
 
+// Unit k of the snake list (k < total).
 template <bool KVOWN>
+__device__ __forceinline__ bool snake_unit(const PrefillParams& p, const UnitSched& sc, int k,
+                                           Unit& w) {
+  const int per_s = p.Hkv * p.npairs;
+  const int ks = k / per_s, rem = k - ks * per_s;
+  int lo = 0, hi = p.n_qt;  // largest qi with pre[qi] <= ks
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sc.pre[mid] <= ks) lo = mid; else hi = mid;
+  }
+  const int g = rem / p.npairs;
+  return decode_unit<KVOWN>(p, lo, sc.ord[ks - sc.pre[lo]], g, rem - g * p.npairs, w);
+}
+
+// The CTA's next unit after round r (advances r). LIST: read from the list decoded in
+// shared memory at the start (units without rows are stored invalid and skipped); else
+// decoded here, which costs a lookup and dependent loads of row offsets at every unit.
+template <bool KVOWN, bool LIST>
 __device__ __forceinline__ bool next_unit(const PrefillParams& p, const UnitSched& sc, int& r,
                                           Unit& w) {
+  if constexpr (LIST) {
+    while (r < sc.n_list) {
+      const int4* u = sc.list + 3 * r++;
+      const int4 a = u[0], b = u[1], e = u[2];
+      if (e.w) {
+        w.start = a.x; w.L = a.y; w.q0 = a.z; w.g = a.w;
+        w.h0 = b.x; w.has1 = b.y; w.kv_lo = b.z; w.n_kv = b.w;
+        w.s = e.x; w.Lk = e.y; w.off = e.z;
+        return true;
+      }
+    }
+    return false;
+  }
   const int G = gridDim.x, c = blockIdx.x;
-  const int per_s = p.Hkv * p.npairs;
   while (true) {
     const int base = r * G;
     if (base >= sc.total) return false;
     const int k = base + (sc.snake && (r & 1) ? G - 1 - c : c);
     ++r;
     if (k >= sc.total) continue;
-    if (!sc.snake) {
-      if (unit_info<KVOWN>(p, k, w)) return true;
-      continue;
-    }
-    const int ks = k / per_s, rem = k - ks * per_s;
-    int lo = 0, hi = p.n_qt;  // largest qi with pre[qi] <= ks
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sc.pre[mid] <= ks) lo = mid; else hi = mid;
-    }
-    const int g = rem / p.npairs;
-    if (decode_unit<KVOWN>(p, lo, sc.ord[ks - sc.pre[lo]], g, rem - g * p.npairs, w)) return true;
+    if (sc.snake ? snake_unit<KVOWN>(p, sc, k, w) : unit_info<KVOWN>(p, k, w)) return true;
   }
 }
 
-template <int D, bool PAGED, bool KVOWN, bool DEFER>
+template <int D, bool PAGED, bool KVOWN, bool DEFER, bool LIST>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -319,8 +347,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const UnitSched sched{ord, pre,
-                        p.snake ? (int)pre[p.n_qt] * p.Hkv * p.npairs : p.total_units, p.snake};
+  const int total_units = p.snake ? (int)pre[p.n_qt] * p.Hkv * p.npairs : p.total_units;
+  UnitSched sched{ord, pre, total_units, p.snake, nullptr, 0};
+  {
+    // Decode the CTA's whole unit list at once (one unit per thread), so that no role pays
+    // the schedule lookup and the dependent row-offset loads at each unit start.
+    const int n_list = (total_units + (int)gridDim.x - 1) / (int)gridDim.x;
+    if constexpr (LIST) {  // the host checked that the snake list fits
+      int4* list = reinterpret_cast<int4*>(smem + S::kList);
+      for (int i = threadIdx.x; i < n_list; i += kThreads) {
+        const int G = gridDim.x, c = blockIdx.x;
+        const int k = i * G + ((i & 1) ? G - 1 - c : c);
+        Unit w{};
+        const bool valid = k < total_units && snake_unit<KVOWN>(p, sched, k, w);
+        list[3 * i] = make_int4(w.start, w.L, w.q0, w.g);
+        list[3 * i + 1] = make_int4(w.h0, w.has1, w.kv_lo, w.n_kv);
+        list[3 * i + 2] = make_int4(w.s, w.Lk, w.off, valid ? 1 : 0);
+      }
+      __syncthreads();
+      sched.list = list;
+      sched.n_list = n_list;
+    } else {
+      (void)n_list;
+    }
+  }
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.err, p.timeout_ns};
   // Paged K/V: each producer warp keeps a window of its unit's page ids in registers,
@@ -440,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kc = 0, vc = 0, qc = 0;
         bool ok = true;
         Unit w;
-        for (int r = 0; ok && next_unit<KVOWN>(p, sched, r, w);) {
+        for (int r = 0; ok && next_unit<KVOWN, LIST>(p, sched, r, w);) {
           const int qs = qc % S::kNQ;
           if (!(ok = wait(bar(S::kBarQEmpty + qs), ((qc / S::kNQ) & 1) ^ 1))) break;
           if (elect_one()) {
@@ -490,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int sf0 = 0, sf1 = 0;  // S issued so far per head tile (s_free phases)
         bool ok = true;
         Unit w;
-        for (int r = 0; ok && next_unit<KVOWN>(p, sched, r, w);) {
+        for (int r = 0; ok && next_unit<KVOWN, LIST>(p, sched, r, w);) {
           const int qs = qc % S::kNQ;
           if (!(ok = wait(bar(S::kBarQFull + qs), (qc / S::kNQ) & 1))) break;
           ++qc;
@@ -539,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int vc = 0, pf = 0, uc = 0;
         bool ok = true;
         Unit w;
-        for (int r = 0; ok && next_unit<KVOWN>(p, sched, r, w);) {
+        for (int r = 0; ok && next_unit<KVOWN, LIST>(p, sched, r, w);) {
           if (t == 1 && !w.has1) {  // this tile is absent: only keep the V ring in step
             vc += w.n_kv;
             continue;
@@ -587,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kc = 0, qc = 0;
       bool ok = true;
       Unit w;
-      for (int r = 0; ok && next_unit<KVOWN>(p, sched, r, w);) {
+      for (int r = 0; ok && next_unit<KVOWN, LIST>(p, sched, r, w);) {
         const int qs = qc % S::kNQ;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(S::kBarQEmpty + qs), ((qc / S::kNQ) & 1) ^ 1, wc));
         if (!ok) break;
@@ -633,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int vc = 0;
       bool ok = true;
       Unit w;
-      for (int r = 0; ok && next_unit<KVOWN>(p, sched, r, w);) {
+      for (int r = 0; ok && next_unit<KVOWN, LIST>(p, sched, r, w);) {
         PageCursor pc{};
         if constexpr (PAGED) cursor_start(pc, w);
         const int krow0 = PAGED ? 0 : key_row0(w);
@@ -686,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait(b, parity, wc));
       };
       Unit w;
-      for (int r = 0; ok && next_unit<KVOWN>(p, sched, r, w);) {
+      for (int r = 0; ok && next_unit<KVOWN, LIST>(p, sched, r, w);) {
         const int n = w.n_kv;
         const int qs = qc % S::kNQ;
         const int nrel = (w.has1 || t == 1) ? 1 : 2;  // commits owed to shared stages
@@ -838,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(S::kBarOFree + t));
     };
     while (ok) {
-      if (!next_unit<KVOWN>(p, sched, r, w)) {
+      if (!next_unit<KVOWN, LIST>(p, sched, r, w)) {
         if constexpr (DEFER) {
           if (pv > 0) {  // the last unit's epilogue
             ok = __all_sync(0xffffffffu, mbar_wait(bar(S::kBarODone + t), (pv - 1) & 1, wc));
@@ -1042,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (stage < 2) named_barrier_sync(kNbTurn + (t ^ 1), 256);
         }
         do {
-          if (!next_unit<KVOWN>(p, sched, r, w)) goto dry_done;
+          if (!next_unit<KVOWN, LIST>(p, sched, r, w)) goto dry_done;
         } while (t == 1 && !w.has1);
         j = 0;
         stage = 0;
@@ -1060,7 +1110,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool PAGED, bool KVOWN, bool DEFER = false>
 cudaError_t launch(const PrefillLaunch& a, const PrefillParams& p, cudaStream_t stream) {
   using S = PrefillSmem<D>;
-  auto kern = prefill_kernel<D, PAGED, KVOWN, DEFER>;
+  const int grid0 = p.total_units < a.num_sms ? p.total_units : a.num_sms;
+  // The CTA's unit list fits in shared memory: the snake schedule is used and even the
+  // bound of every (q tile, sequence) pair being valid leaves at most kMaxListUnits per CTA.
+  const bool list = S::kMaxListUnits > 0 && p.snake &&
+                    (p.total_units + grid0 - 1) / grid0 <= S::kMaxListUnits;
+  auto kern = list ? prefill_kernel<D, PAGED, KVOWN, DEFER, (D == 64)>
+                   : prefill_kernel<D, PAGED, KVOWN, DEFER, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.total_units < a.num_sms ? p.total_units : a.num_sms;

@@ -66,6 +66,12 @@ CASES = {
     "D128 G8 sinks N(0,1)": lambda: wl.prefill_case([200, 385], 8, 1, 128, seed=6),
     "D128 G16 W64": lambda: wl.prefill_case([260, 64, 1], 16, 1, 128, window=64, seed=7),
     "D128 G4 W1000 ragged": lambda: wl.prefill_case([1000, 1001, 77], 8, 2, 128, window=1000, seed=8),
+    # the bound on units per CTA (every q tile of the longest sequence in every sequence,
+    # 32 x 100 x 8 x 4 / 152 = 674) exceeds the 512 the shared-memory unit list holds:
+    # head_dim 64 then decodes each unit when it starts
+    "100 sequences, one of 4096, D64 G8": lambda: wl.prefill_case(
+        [4096] + [int(x) for x in np.random.default_rng(17).integers(1, 100, 99)], 64, 8, 64,
+        seed=17),
     # more sequences than the snake schedule's tables hold: round-robin over all unit ids
     "130 sequences D64 G2": lambda: wl.prefill_case(
         [int(x) for x in np.random.default_rng(16).integers(0, 200, 130)], 4, 2, 64, seed=16),
