@@ -51,10 +51,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by the SHA-256 of the kernel source it was taken on; stale entries are ignored.
 NCU_TRAFFIC = {
-    # prefill_kernel<64,0,0,0>, gpt-oss causal: 194.7 MB read + 116.9 MB written
-    "prefill_tc.cu:aff689f36a498461": 311.6e6,
-    # decode_split_kernel<64,1,false,8>, gpt-oss decode: 691.5 MB read + 7.8 MB written
-    "decode_split.cu:50fd510972eaccab": 699.4e6,
+    # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 195.6 MB read + 116.5 MB written
+    "prefill_tc.cu:a31c1311d91e3fd6": 312.1e6,
+    # decode_split_kernel<64,1,false,8>, gpt-oss decode: 691.5 MB read + 7.3 MB written
+    "decode_split.cu:fead54c850f5b7b4": 698.8e6,
 }
 
 
@@ -486,7 +486,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak_tc,
                      "unit": "TFLOP/s", "frac": round(tflops / peak_tc, 4),
                      "traffic": traffic("prefill_tc.cu"),
-                     "kernel": "prefill_kernel<64,0,0> (gpt-oss causal)",
+                     "kernel": "prefill_kernel<64,0,0,0,1> (gpt-oss causal)",
                      "peak_source": f"bf16_tflops burst, {peak_src}"},
         "prefill_window128": {"value": round(tflops_w, 3), "unit": "TFLOP/s",
                               "frac": round(tflops_w / peak_tc, 4),

@@ -175,11 +175,12 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       const int32_t* pt = p.page_table + (size_t)b * p.max_pages + p_first;
       int cur = lane < npg ? pt[lane] : -1;
       int nxt = 32 + lane < npg ? pt[32 + lane] : -1;
-      int issued = 0;
-      // Test switch: page 0 of (chunk 0, kv head 0, sequence 0) is never copied, so the
-      // consumers' bounded wait for it runs out and the CTA aborts through its normal path.
-      const bool withheld = p.withhold && c == 0 && g == 0 && b == 0;
-      for (int i = 0; i < npg; ++i) {
+      // Test switch: page 0 of (chunk 0, kv head 0, sequence 0) is never copied (the loop
+      // starts at page 1), so the consumers' bounded wait for it runs out and the CTA
+      // aborts through its normal path.
+      const int first = (p.withhold && c == 0 && g == 0 && b == 0) ? 1 : 0;
+      int issued = first;
+      for (int i = first; i < npg; ++i) {
         if (i > 0 && (i & 31) == 0) {
           cur = nxt;
           nxt = i + 32 + lane < npg ? pt[i + 32 + lane] : -1;
@@ -188,7 +189,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
         const int st = i % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * st, ((i / kStages) & 1) ^ 1, wc)))
           break;
-        if (elect_one() && !(withheld && i == 0)) {
+        if (elect_one()) {
           const uint32_t full = bar_full + 8 * st;
           if (pid < 0 || pid >= p.num_pages) {
             atomicOr(p.err, kErrPageId);
@@ -215,10 +216,8 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
       }
       // Let every copy still in flight land before the CTA can exit.
       if (lane == 0) {
-        for (int i = max(0, issued - kStages); i < issued; ++i) {
-          if (withheld && i == 0) continue;  // no copy was issued for it
+        for (int i = max(first, issued - kStages); i < issued; ++i)  // pages copied
           mbar_drain(bar_full + 8 * (i % kStages), (i / kStages) & 1, p.drain_ns);
-        }
       }
     }
     return;
@@ -532,6 +531,16 @@ __global__ void __launch_bounds__(kDecodeThreads, F8 ? 3 : 4)
   decode_split_body<D, NT, F8, ST>(tm_k, tm_v, p);
 }
 
+// FP8 cache at head_dim 64 with one head tile: capped for seven CTAs per SM (56 registers),
+// the residency its shared memory allows; left to itself the compiler takes 60, which
+// leaves room for six.
+template <int D, int NT, bool F8, int ST>
+__global__ void __launch_bounds__(kDecodeThreads, 7)
+    decode_split_kernel_7(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  decode_split_body<D, NT, F8, ST>(tm_k, tm_v, p);
+}
+
 // One warp per (sequence, query head): out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).
 // Launched as a programmatic dependent of the split kernel; chunk rows are read eight at a
 // time so their loads overlap instead of forming a dependent chain.
@@ -599,6 +608,7 @@ cudaError_t launch_split_ring(const DecodeLaunch& a, const DecodeParams& p, cuda
   using S = DecodeSmem<D, NT, F8, ST>;
   auto kern = []() {
     if constexpr (NT == 2 && D == 128) return decode_split_kernel_3<D, NT, F8, ST>;
+    else if constexpr (F8 && NT == 1 && D == 64) return decode_split_kernel_7<D, NT, F8, ST>;
     else return decode_split_kernel<D, NT, F8, ST>;
   }();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
