@@ -90,7 +90,8 @@ struct PrefillSmem {
   static constexpr int kBoxBytes = 128 * 128;      // 128 rows x 128 bytes
   static constexpr int kTileBytes = 128 * D * 2;   // one Q, K or V tile
   static constexpr int kNQ = (D == 64) ? 2 : 1;    // Q ring depth (a stage holds both head tiles)
-  static constexpr int kNK = (D == 64) ? 4 : 3;    // K ring depth
+  static constexpr int kNK = (D == 64) ? 4 : 2;    // K ring depth (head_dim 128: 3 -> 2 measured
+                                                   // 0.5% faster and frees room for the unit list)
   static constexpr int kNV = (D == 64) ? 4 : 2;    // V ring depth
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kNQ * 2 * kTileBytes;
@@ -109,12 +110,12 @@ struct PrefillSmem {
   // Windowed head_dim 64: each softmax thread's pending epilogue (row, 1/d, log-sum-exp).
   static constexpr int kPend = (kPre + 2 * (kMaxSchedQTiles + 1) + 15) / 16 * 16;
   static constexpr int kPendBytes = (D == 64) ? 2 * 128 * 16 : 0;
-  // head_dim 64: the CTA's units, decoded once at the start (48 bytes each; head_dim 128
-  // has no room left and decodes each unit when it starts). Window 128: 152 -> 129 us,
-  // causal 0.765 -> 0.743 ms: the lookup and the row-offset loads sat in every unit start.
+  // The CTA's units, decoded once at the start (48 bytes each). Window 128: 152 -> 129 us,
+  // causal 0.765 -> 0.743 ms, Qwen3-235B-style head_dim 128 0.741 -> 0.735 ms: the lookup and
+  // the row-offset loads sat in every unit start.
   // (Addressing the list through a 32-bit shared address moved the kernel's few spilled
   // registers into the step loop and lost the gain: 0.764 ms.)
-  static constexpr int kMaxListUnits = (D == 64) ? 512 : 0;
+  static constexpr int kMaxListUnits = 512;
   static constexpr int kList = (kPend + kPendBytes + 15) / 16 * 16;
   static constexpr int kBytes = kList + kMaxListUnits * 48 + 1024;  // + alignment slack
   static_assert(kBytes <= 232448, "shared memory per CTA");
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int npad = 1;
       while (npad < n_pairs) npad <<= 1;
       unsigned long long* key = reinterpret_cast<unsigned long long*>(smem + S::kK + 4096);
-      static_assert(4096 + 8 * kMaxSortPairs <= S::kNK * S::kTileBytes || D != 64,
+      static_assert(4096 + 8 * kMaxSortPairs <= S::kNK * S::kTileBytes,
                     "the pair keys must fit in the K ring");
       const bool sorted = (PAGED || KVOWN) && npad <= kMaxSortPairs;
       if (sorted) {
@@ -1168,7 +1169,7 @@ cudaError_t launch(const PrefillLaunch& a, const PrefillParams& p, cudaStream_t 
   // bound of every (q tile, sequence) pair being valid leaves at most kMaxListUnits per CTA.
   const bool list = S::kMaxListUnits > 0 && p.snake &&
                     (p.total_units + grid0 - 1) / grid0 <= S::kMaxListUnits;
-  auto kern = list ? prefill_kernel<D, PAGED, KVOWN, DEFER, (D == 64)>
+  auto kern = list ? prefill_kernel<D, PAGED, KVOWN, DEFER, true>
                    : prefill_kernel<D, PAGED, KVOWN, DEFER, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
   if (e != cudaSuccess) return e;

@@ -72,6 +72,9 @@ CASES = {
     "100 sequences, one of 4096, D64 G8": lambda: wl.prefill_case(
         [4096] + [int(x) for x in np.random.default_rng(17).integers(1, 100, 99)], 64, 8, 64,
         seed=17),
+    "100 sequences, one of 4096, D128 G8": lambda: wl.prefill_case(
+        [4096] + [int(x) for x in np.random.default_rng(18).integers(1, 100, 99)], 64, 8, 128,
+        seed=18),
     # more sequences than the snake schedule's tables hold: round-robin over all unit ids
     "130 sequences D64 G2": lambda: wl.prefill_case(
         [int(x) for x in np.random.default_rng(16).integers(0, 200, 130)], 4, 2, 64, seed=16),
