@@ -51,8 +51,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by the SHA-256 of the kernel source it was taken on; stale entries are ignored.
 NCU_TRAFFIC = {
-    # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 195.6 MB read + 116.5 MB written
-    "prefill_tc.cu:a31c1311d91e3fd6": 312.1e6,
+    # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 194.8 MB read + 117.4 MB written
+    "prefill_tc.cu:ea5628ff9107a472": 312.2e6,
     # decode_split_kernel<64,1,false,8>, gpt-oss decode: 691.5 MB read + 7.3 MB written
     "decode_split.cu:fead54c850f5b7b4": 698.8e6,
 }
