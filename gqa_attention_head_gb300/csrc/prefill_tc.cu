@@ -25,6 +25,8 @@
 //   head_dim 128 warp 0 loads Q and K, warp 2 loads V (its own ring, so K never waits
 //                behind V); warps 1 and 3 each issue both MMAs of one head tile, in the order
 //                PV_t(j-1) then S_t(j), because P_t overwrites S_t's columns.
+//   paged K/V at head_dim 64 takes the head_dim-128 roles, with S_t(j+1) issued before
+//                PV_t(j) (P_t has its own columns there).
 // All stages are 128-byte swizzled; warp 1 allocates the 512 TMEM columns.
 // Warps 4-7 are the softmax warpgroup of head tile 0, warps 8-11 that of head tile 1;
 // thread r owns row r (TMEM lane r): masks, runs the online softmax in the exp2 domain
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // head_dim 128 has one issuer per head tile for everything.
       const bool q_or_k = (i >= S::kBarQEmpty && i < S::kBarQEmpty + S::kNQ) ||
                           (i >= S::kBarKEmpty && i < S::kBarKEmpty + S::kNK);
-      const bool by_issuers = (!TmemCols<D>::kSepP && q_or_k) ||
+      const bool by_issuers = ((!TmemCols<D>::kSepP || PAGED) && q_or_k) ||
                               (i >= S::kBarVEmpty && i < S::kBarVEmpty + S::kNV);
       mbar_init(bar(i), by_threads ? 128 : by_issuers ? 2 : 1);
     }
@@ -523,7 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     regs_dealloc<kRegsLow>();
-    if constexpr (TmemCols<D>::kSepP) {
+    // head_dim 64: one producer for Q, K and V, one S issuer for both head tiles and one PV
+    // issuer per tile. Paged K/V (sixteen 16-row page copies per step) use the head_dim-128
+    // roles instead (Q and K from warp 0, V from warp 2, one S+PV issuer per tile): there a
+    // single producer falls behind (chunked gpt-oss prefill 0.658 -> 0.619 ms), while the
+    // contiguous calls are faster this way (causal 0.754 -> 0.744 ms).
+    if constexpr (TmemCols<D>::kSepP && !PAGED) {
       using C = TmemCols<D>;
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, false, true);
