@@ -51,8 +51,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by the SHA-256 of the kernel source it was taken on; stale entries are ignored.
 NCU_TRAFFIC = {
-    # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 194.8 MB read + 117.4 MB written
-    "prefill_tc.cu:ea5628ff9107a472": 312.2e6,
+    # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 194.8 MB read + 117.0 MB written
+    "prefill_tc.cu:c64132d724481f28": 311.8e6,
     # decode_split_kernel<64,1,false,8>, gpt-oss decode: 691.5 MB read + 7.3 MB written
     "decode_split.cu:fead54c850f5b7b4": 698.8e6,
 }
