@@ -444,7 +444,7 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");  // ring is free now
   if (*abort_flag) aborted = true;
   constexpr int GP = NTW * 8;  // heads held per warp (padded)
-  static_assert(kConsumerWarps * GP * (2 + D) * 4 <= S::kRingBytes,
+  static_assert((kConsumerWarps * GP * (2 + D) + 16 * kConsumerWarps) * 4 <= S::kRingBytes,
                 "the combine scratch must fit in the ring it reuses");
   float* cm = reinterpret_cast<float*>(smem);  // [4][GP]
   float* cl = cm + kConsumerWarps * GP;        // [4][GP]
@@ -480,35 +480,62 @@ __device__ __forceinline__ void decode_split_body(const CUtensorMap& tm_k, const
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
   if (aborted) return;
 
-  const bool with_sink = (c == 0) && (p.sinks != nullptr);
-  for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
-    const int hl = idx / D, d = idx % D;
+  // Per head: each holding warp's weight 2^(m_w - M) / d (the sink counted once, in the
+  // first chunk of the visible range) and the chunk's log-sum-exp, once per head instead of
+  // once per output element.
+  constexpr int NW = kSplitTiles ? 2 : kConsumerWarps;  // warps holding one head
+  float* cwt = co + kConsumerWarps * GP * D;            // [G][NW]
+  if (threadIdx.x < G) {
+    const int hl = threadIdx.x;
     const int h = head0 + hl;
-    // the warps holding head hl, and its index among their heads
-    constexpr int NW = kSplitTiles ? 2 : kConsumerWarps;
     const int w0 = kSplitTiles ? 2 * (hl >> 3) : 0;
     const int hh = kSplitTiles ? (hl & 7) : hl;
-    const float sink_l2 = with_sink ? p.sinks[h] * kLog2e : -INFINITY;
+    const float sink_l2 = (c == 0 && p.sinks != nullptr) ? p.sinks[h] * kLog2e : -INFINITY;
     float M = sink_l2;
 #pragma unroll
-    for (int w = w0; w < w0 + NW; ++w) M = fmaxf(M, cm[w * GP + hh]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, cm[(w0 + w) * GP + hh]);
     const float Mu = M == -INFINITY ? 0.f : M;
     float lsum = ex2(sink_l2 - Mu);
-    float acc = 0.f;
+    float f[NW];
 #pragma unroll
-    for (int w = w0; w < w0 + NW; ++w) {
-      const float f = ex2(cm[w * GP + hh] - Mu);
-      lsum += cl[w * GP + hh] * f;
-      acc += co[(w * GP + hh) * D + d] * f;
+    for (int w = 0; w < NW; ++w) {
+      f[w] = ex2(cm[(w0 + w) * GP + hh] - Mu);
+      lsum += cl[(w0 + w) * GP + hh] * f[w];
     }
-    const float val = lsum > 0.f ? acc / lsum : 0.f;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) cwt[hl * NW + w] = f[w] * inv;
     const size_t bh = (size_t)b * p.Hq + h;
     if (nch == 1) {
-      p.out[bh * D + d] = __float2bfloat16_rn(val);
-      if (d == 0 && p.lse_out) p.lse_out[bh] = lsum > 0.f ? (Mu + log2f(lsum)) * kLn2 : -INFINITY;
+      if (p.lse_out) p.lse_out[bh] = lsum > 0.f ? (Mu + log2f(lsum)) * kLn2 : -INFINITY;
     } else {
-      p.o_part[(bh * p.cmax + c) * D + d] = val;
-      if (d == 0) p.lse_part[bh * p.cmax + c] = lsum > 0.f ? Mu + __log2f(lsum) : -INFINITY;
+      p.lse_part[bh * p.cmax + c] = lsum > 0.f ? Mu + __log2f(lsum) : -INFINITY;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+  // The weighted sums, four consecutive head_dim elements per thread.
+  for (int idx = threadIdx.x; idx < G * D / 4; idx += kConsumerWarps * 32) {
+    const int hl = idx / (D / 4), d = 4 * (idx % (D / 4));
+    const int w0 = kSplitTiles ? 2 * (hl >> 3) : 0;
+    const int hh = kSplitTiles ? (hl & 7) : hl;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = cwt[hl * NW + w];
+      const float4 x = *reinterpret_cast<const float4*>(co + ((w0 + w) * GP + hh) * D + d);
+      acc.x += x.x * f;
+      acc.y += x.y * f;
+      acc.z += x.z * f;
+      acc.w += x.w * f;
+    }
+    const size_t bh = (size_t)b * p.Hq + head0 + hl;
+    if (nch == 1) {
+      uint2 v;
+      v.x = pack_bf16x2(acc.x, acc.y);
+      v.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(p.out + bh * D + d) = v;
+    } else {
+      *reinterpret_cast<float4*>(p.o_part + (bh * p.cmax + c) * D + d) = acc;
     }
   }
 }
