@@ -16,8 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libsink_attn.so")
-SOURCES = ["sink_attn_api.cu", "prefill_tc.cu", "decode_split.cu", "decode_static_ws.cu",
-           "merge_states.cu", "kv_append.cu"]
+SOURCES = ["sink_attn_api.cu", "prefill_tc.cu", "prefill_band.cu", "decode_split.cu",
+           "decode_static_ws.cu", "merge_states.cu", "kv_append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -24,7 +24,25 @@ struct PrefillLaunch {
   float scale;
   int num_sms;
   uint64_t timeout_ns;
+  int band;                      // the short-window kernel: tm_q has box {64, 4, 32} and
+                                 // tm_k/tm_v box {64, 1, 160} (prefill_band_applies)
 };
+
+// The short-window prefill kernel (prefill_band.cu): 32 queries x 8 query heads per unit,
+// each unit reading one 160-key span. It serves contiguous head_dim-64 calls with a window
+// of 1..128 keys when every kv head has a multiple of 8 query heads, up to kBandMaxSeqs
+// sequences and kBandMaxUnits units per CTA (bounded here from the row count).
+constexpr int kBandMaxSeqs = 1024;
+constexpr int kBandMaxUnits = 512;
+inline bool prefill_band_applies(int head_dim, int window, int num_q_heads, int num_kv_heads,
+                                 long long total_tokens, int num_seqs, int num_sms) {
+  if (head_dim != 64 || window <= 0 || window > 128 || num_sms <= 0) return false;
+  if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
+  const int g = num_q_heads / num_kv_heads;
+  if (g % 8 != 0 || num_seqs <= 0 || num_seqs > kBandMaxSeqs) return false;
+  const long long blocks = total_tokens / 32 + num_seqs;  // query blocks of 32, at most
+  return blocks * num_kv_heads * (g / 8) <= (long long)kBandMaxUnits * num_sms;
+}
 
 struct DecodeLaunch {
   CUtensorMap tm_k, tm_v;        // 2-D maps {head_dim, pages*Hkv*page_size}, box {64, 16};
@@ -93,6 +111,7 @@ struct QuantizeLaunch {
 };
 
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream);
+cudaError_t launch_prefill_band(const PrefillLaunch& a, cudaStream_t stream);
 cudaError_t launch_quantize_fp8(const QuantizeLaunch& a, cudaStream_t stream);
 cudaError_t launch_append_kv(const AppendLaunch& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);

@@ -1188,6 +1188,7 @@ cudaError_t launch(const PrefillLaunch& a, const PrefillParams& p, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream) {
+  if (a.band) return launch_prefill_band(a, stream);
   PrefillParams p{};
   p.cu = a.cu_seqlens;
   p.sinks = a.sinks;

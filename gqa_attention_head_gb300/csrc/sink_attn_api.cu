@@ -83,15 +83,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// bf16 [rows][heads][dim] as a 3-D map {dim, heads, rows}, box {64, 1, box_rows},
-// 128-byte swizzle (each box row is exactly 128 bytes).
+// bf16 [rows][heads][dim] as a 3-D map {dim, heads, rows}, box {64, box_heads, box_rows},
+// 128-byte swizzle (each box row is exactly 128 bytes; a box lands as box_rows x box_heads
+// rows of 128 bytes, heads fastest).
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t dim, uint64_t heads, uint64_t rows,
-               uint32_t box_rows) {
+               uint32_t box_rows, uint32_t box_heads = 1) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t gdim[3] = {dim, heads, rows};
   cuuint64_t gstride[2] = {dim * 2, heads * dim * 2};
-  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t box[3] = {64, box_heads, box_rows};
   cuuint32_t estride[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -205,13 +206,21 @@ sink_attn_status prefill_impl(const sink_attn_bf16* q, const sink_attn_bf16* k,
   if (n_qt * num_seqs * num_q_heads >= ((int64_t)1 << 31)) return SINK_ATTN_ERR_UNSUPPORTED;
 
   sa::PrefillLaunch a{};
-  if (!encode_3d(&a.tm_q, q, head_dim, num_q_heads, total_tokens, 128) ||
-      !encode_3d(&a.tm_k, k, head_dim, num_kv_heads, rows_k, 128) ||
-      !encode_3d(&a.tm_v, v, head_dim, num_kv_heads, rows_k, 128))
-    return SINK_ATTN_ERR_CUDA;
   a.err = device_error_word();
   a.num_sms = num_sms_current();
   if (!a.err || a.num_sms <= 0) return SINK_ATTN_ERR_CUDA;
+  a.band = (!kv_own && sa::prefill_band_applies(head_dim, window, num_q_heads, num_kv_heads,
+                                                total_tokens, num_seqs, a.num_sms))
+               ? 1
+               : 0;
+  const bool maps_ok =
+      a.band ? encode_3d(&a.tm_q, q, head_dim, num_q_heads, total_tokens, 32, 4) &&
+                   encode_3d(&a.tm_k, k, head_dim, num_kv_heads, rows_k, 160) &&
+                   encode_3d(&a.tm_v, v, head_dim, num_kv_heads, rows_k, 160)
+             : encode_3d(&a.tm_q, q, head_dim, num_q_heads, total_tokens, 128) &&
+                   encode_3d(&a.tm_k, k, head_dim, num_kv_heads, rows_k, 128) &&
+                   encode_3d(&a.tm_v, v, head_dim, num_kv_heads, rows_k, 128);
+  if (!maps_ok) return SINK_ATTN_ERR_CUDA;
   a.cu_seqlens = cu_seqlens;
   a.kv_lens = nullptr;
   a.page_table = nullptr;

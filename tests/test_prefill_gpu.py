@@ -78,6 +78,21 @@ CASES = {
     # more sequences than the snake schedule's tables hold: round-robin over all unit ids
     "130 sequences D64 G2": lambda: wl.prefill_case(
         [int(x) for x in np.random.default_rng(16).integers(0, 200, 130)], 4, 2, 64, seed=16),
+    # short windows at head_dim 64 with groups of 8k query heads: the kernel whose unit is 32
+    # queries x 8 heads over one 160-key span (lengths around its 32-row blocks, spans that
+    # reach into the previous sequence or before the first row, empty sequences)
+    "band D64 G8 W128 ragged": lambda: wl.prefill_case(
+        [1, 31, 32, 33, 127, 128, 129, 300, 0, 513], 16, 2, 64, window=128, seed=21),
+    "band D64 G8 W1": lambda: wl.prefill_case([5, 130, 257], 8, 1, 64, window=1, seed=22),
+    "band D64 G16 W100": lambda: wl.prefill_case([260, 64, 1, 97], 32, 2, 64, window=100,
+                                                 seed=23),
+    "band D64 G8 W33 no sinks": lambda: wl.prefill_case([200, 45], 8, 1, 64, window=33,
+                                                        sinks=None, seed=24),
+    "band D64 G8 W128 sinks -inf": lambda: wl.prefill_case([400], 8, 1, 64, window=128,
+                                                           sinks="-inf", seed=25),
+    "band 300 sequences D64 G8 W64": lambda: wl.prefill_case(
+        [int(x) for x in np.random.default_rng(26).integers(0, 200, 300)], 8, 1, 64, window=64,
+        seed=26),
 }
 
 
@@ -104,17 +119,19 @@ def test_prefill_rescale_path():
     assert_clean_device()
 
 
-def test_prefill_large_sink_gives_zero():
-    case = wl.prefill_case([300, 50], 8, 2, 64, sinks=1.0e4, seed=10)
+@pytest.mark.parametrize("hkv,window", [(2, 0), (1, 128)])
+def test_prefill_large_sink_gives_zero(hkv, window):
+    case = wl.prefill_case([300, 50], 8, hkv, 64, sinks=1.0e4, window=window, seed=10)
     got = gpu_prefill(case)
     assert torch.count_nonzero(got.float()) == 0
     assert_clean_device()
 
 
-def test_prefill_guard_bands_and_foreign_rows_untouched():
+@pytest.mark.parametrize("hkv,window", [(2, 0), (1, 128)])
+def test_prefill_guard_bands_and_foreign_rows_untouched(hkv, window):
     """Rows of tokens outside every sequence, and guard rows around `out`, keep their
     sentinel: the kernel writes only the rows it owns."""
-    case = wl.prefill_case([129, 40], 8, 2, 64, seed=11, extra_tokens=7)
+    case = wl.prefill_case([129, 40], 8, hkv, 64, window=window, seed=11, extra_tokens=7)
     T = case.total_tokens
     guard = 64
     big = torch.full((T + 2 * guard, 8, 64), -7.25, dtype=torch.bfloat16, device="cuda")
@@ -127,13 +144,15 @@ def test_prefill_guard_bands_and_foreign_rows_untouched():
     assert_clean_device()
 
 
-@pytest.mark.parametrize("d,window", [(64, 0), (128, 0), (64, 128), (128, 50)])
-def test_prefill_out_16_byte_aligned_matches_32_byte_aligned(d, window):
+@pytest.mark.parametrize("d,window,hkv", [(64, 0, 2), (128, 0, 2), (64, 128, 2), (128, 50, 2),
+                                           (64, 128, 1)])
+def test_prefill_out_16_byte_aligned_matches_32_byte_aligned(d, window, hkv):
     """Output rows go out as 32-byte stores when `out` is 32-byte aligned, as 16-byte stores
     when it is only 16-byte aligned (what the interface requires): the two give the same
     bits, and the bytes around the offset buffer keep their sentinel. Windowed head_dim 64
-    runs the kernel form whose epilogue is deferred into the next unit."""
-    case = wl.prefill_case([129, 300, 40], 8, 2, d, window=window, seed=13, extra_tokens=5)
+    runs the kernel form whose epilogue is deferred into the next unit (groups of 4) or the
+    short-window kernel (groups of 8)."""
+    case = wl.prefill_case([129, 300, 40], 8, hkv, d, window=window, seed=13, extra_tokens=5)
     n = case.total_tokens * 8 * d
     ref = gpu_prefill(case)
     assert ref.data_ptr() % 32 == 0
