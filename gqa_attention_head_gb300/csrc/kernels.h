@@ -26,6 +26,7 @@ struct PrefillLaunch {
   uint64_t timeout_ns;
   int band;                      // the short-window kernel: tm_q has box {64, 4, 32} and
                                  // tm_k/tm_v box {64, 1, 160} (prefill_band_applies)
+  CUtensorMap tm_o;              // band: `out` as {head_dim, heads, tokens}, box {64, 4, 32}
 };
 
 // The short-window prefill kernel (prefill_band.cu): 32 queries x 8 query heads per unit,

@@ -46,6 +46,7 @@ constexpr uint32_t kRegsHigh = 216;  // softmax warpgroups
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kNbTeardown = 1;
 constexpr uint32_t kNbTurn = 2;  // + t: softmax warpgroup t may take its turn (256 threads)
+constexpr uint32_t kNbEpi = 4;   // + t: the 128 threads of softmax warpgroup t (output staging)
 
 // Turn hand-overs between the two softmax warpgroups carry no data (each touches only its own
 // TMEM columns), so these forms do not clobber memory; being volatile they stay in order with
@@ -60,11 +61,12 @@ __device__ __forceinline__ void turn_pass(uint32_t id) {
 struct BandSmem {
   static constexpr int kQTile = 128 * 128;     // one head tile of Q: 128 rows x 128 bytes
   static constexpr int kKVTile = kSpan * 128;  // one K or V span: 160 rows x 128 bytes
-  static constexpr int kNQ = 2, kNK = 3, kNV = 3;
+  static constexpr int kNQ = 2, kNK = 2, kNV = 2;
   static constexpr int kQ = 0;  // [kNQ][2 head tiles]
   static constexpr int kK = kQ + kNQ * 2 * kQTile;
   static constexpr int kV = kK + kNK * kKVTile;
-  static constexpr int kBar = kV + kNV * kKVTile;
+  static constexpr int kO = kV + kNV * kKVTile;  // [2 head tiles]: output rows for the TMA store
+  static constexpr int kBar = kO + 2 * kQTile;
   static constexpr int kBarQFull = 0, kBarQEmpty = kBarQFull + kNQ, kBarKFull = kBarQEmpty + kNQ,
                        kBarKEmpty = kBarKFull + kNK, kBarVFull = kBarKEmpty + kNK,
                        kBarVEmpty = kBarVFull + kNV, kBarSFull = kBarVEmpty + kNV,  // [2]
@@ -101,13 +103,15 @@ struct BandUnit {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_band_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const BandParams p) {
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_o, const BandParams p) {
   using S = BandSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sb = smem_addr(smem);
   const uint32_t q_smem = sb + S::kQ, k_smem = sb + S::kK, v_smem = sb + S::kV;
+  const uint32_t o_smem = sb + S::kO;
   auto bar = [&](int i) -> uint32_t { return sb + S::kBar + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kMisc + 4);
@@ -364,9 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before the query, inside the window, and not before the sequence's first row).
       const int hi = tok + 128;
       const int lo = max(128 - u.q0, tok + 129 - p.window);
+      // Columns 32..127 are visible to every row of the unit when the window is 128 keys and
+      // the span starts at or after the sequence's first row plus 32 (q0 >= 96): then only
+      // the first and the last 32 columns are masked.
+      const bool mid_visible = u.q0 >= 96 && p.window >= 128;
       // One visibility word per 32 columns, then one bit test per column.
 #pragma unroll
       for (int b = 0; b < kSpan / 32; ++b) {
+        if (b != 0 && b != kSpan / 32 - 1 && mid_visible) continue;
         const int hc = min(max(hi, 32 * b - 1), 32 * b + 31) - 32 * b;  // -1 .. 31
         const int lc = min(max(lo, 32 * b), 32 * b + 32) - 32 * b;      // 0 .. 32
         const uint32_t vis =
@@ -416,23 +425,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = d > 0.f ? 1.f / d : 0.f;
       const bool row_ok = qi < u.len;
       const size_t orow = (size_t)(u.start + qi) * p.Hq + h;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (row_ok ? orow : 0) * kD);
+      if (u.len - u.q0 >= kQB) {
+        // A whole block of 32 queries: the rows go to shared memory in the layout of the
+        // output box (row = 4 * query + head, 128-byte swizzle) and leave in one TMA store per
+        // head tile, instead of 128 threads storing 128 bytes each.
+        const uint32_t obuf = o_smem + t * S::kQTile;
+        if (row == 0) bulk_wait_group_read0();  // this tile's previous store has read obuf
+        named_barrier_sync(kNbEpi + t, 128);
 #pragma unroll
-      for (int c4 = 0; c4 < kD / 32; ++c4) {
-        uint32_t o[32];
-        tmem_ld32(to + 32 * c4, o);
-        uint32_t q16[16];
+        for (int c4 = 0; c4 < kD / 32; ++c4) {
+          uint32_t o[32];
+          tmem_ld32(to + 32 * c4, o);
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          q16[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-        if (row_ok) {
-          if (p.out32) {
+          for (int e = 0; e < 4; ++e) {
+            uint32_t w4[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) st_global_v8(dst + c4 * 4 + 2 * e, &q16[8 * e]);
-          } else {
+            for (int k2 = 0; k2 < 4; ++k2)
+              w4[k2] = pack_bf16x2(__uint_as_float(o[8 * e + 2 * k2]) * inv,
+                                   __uint_as_float(o[8 * e + 2 * k2 + 1]) * inv);
+            const int chunk = 4 * c4 + e;  // 16-byte chunk of the 128-byte row
+            const uint32_t a = obuf + row * 128 + ((chunk ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w4[0]),
+                         "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                         : "memory");
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        named_barrier_sync(kNbEpi + t, 128);
+        if (row == 0) {
+          tma_store_3d(&tm_o, obuf, 0, (u.go & 0xffff) * p.G + 8 * (u.go >> 16) + 4 * t,
+                       u.start + u.q0);
+          bulk_commit_group();
+        }
+      } else {
+        // The sequence's last, partial block: per-row stores, rows of this sequence only.
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (row_ok ? orow : 0) * kD);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[c4 * 4 + e] = make_uint4(q16[4 * e], q16[4 * e + 1], q16[4 * e + 2], q16[4 * e + 3]);
+        for (int c4 = 0; c4 < kD / 32; ++c4) {
+          uint32_t o[32];
+          tmem_ld32(to + 32 * c4, o);
+          uint32_t q16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            q16[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+          if (row_ok) {
+            if (p.out32) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) st_global_v8(dst + c4 * 4 + 2 * e, &q16[8 * e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[c4 * 4 + e] = make_uint4(q16[4 * e], q16[4 * e + 1], q16[4 * e + 2], q16[4 * e + 3]);
+            }
           }
         }
       }
@@ -447,14 +491,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Dry tail: the remaining turn hand-overs of this warpgroup's list, all blocking, so
       // that the partner warpgroup (which aborts as well, its waits seeing the abort flag)
       // never waits on a turn that does not come.
+      // The output staging barriers of whole blocks are met the same way (a warp aborts only
+      // in a wait before its turn or before its epilogue).
       for (; i < n_list; ++i, stage = 0) {
-        if (list[i].y == 0) continue;
+        const int4 e = list[i];
+        if (e.y == 0) continue;
         if (stage < 1) turn_wait(kNbTurn + t);
         if (stage < 2) turn_pass(kNbTurn + (t ^ 1));
+        if (e.y - e.z >= kQB) {
+          named_barrier_sync(kNbEpi + t, 128);
+          named_barrier_sync(kNbEpi + t, 128);
+        }
       }
     }
     // Warpgroup 1's hand-overs lead warpgroup 0's turns by one: take the last.
     if (t == 0) turn_wait(kNbTurn + 0);
+    if (row == 0) bulk_wait_group0();  // this tile's output stores are complete
     __syncwarp();
     tc_fence_before_sync();
     named_barrier_sync(kNbTeardown, kThreads);
@@ -484,7 +536,8 @@ cudaError_t launch_prefill_band(const PrefillLaunch& a, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(prefill_band_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
   if (e != cudaSuccess) return e;
-  prefill_band_kernel<<<a.num_sms, kThreads, S::kBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, p);
+  prefill_band_kernel<<<a.num_sms, kThreads, S::kBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o,
+                                                                  p);
   return cudaGetLastError();
 }
 
