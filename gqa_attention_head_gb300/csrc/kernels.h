@@ -24,13 +24,13 @@ struct PrefillLaunch {
   float scale;
   int num_sms;
   uint64_t timeout_ns;
-  int band;                      // the short-window kernel: tm_q has box {64, 4, 32} and
+  int band;                      // the short-window kernel: tm_q has box {64, 8, 16} and
                                  // tm_k/tm_v box {64, 1, 160} (prefill_band_applies)
-  CUtensorMap tm_o;              // band: `out` as {head_dim, heads, tokens}, box {64, 4, 32}
+  CUtensorMap tm_o;              // band: `out` as {head_dim, heads, tokens}, box {64, 8, 16}
 };
 
-// The short-window prefill kernel (prefill_band.cu): 32 queries x 8 query heads per unit,
-// each unit reading one 160-key span. It serves contiguous head_dim-64 calls with a window
+// The short-window prefill kernel (prefill_band.cu): 32 queries x 8 query heads per unit
+// (two head tiles of 16 queries x 8 heads), each unit reading one 160-key span. It serves contiguous head_dim-64 calls with a window
 // of 1..128 keys when every kv head has a multiple of 8 query heads, up to kBandMaxSeqs
 // sequences and kBandMaxUnits units per CTA (bounded here from the row count).
 constexpr int kBandMaxSeqs = 1024;

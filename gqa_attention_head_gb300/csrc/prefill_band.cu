@@ -3,14 +3,15 @@
 // every other layer attending to a 128-token window; "GPT-OSS am Day 0", §Sink-Attention).
 //
 // Work unit: 32 consecutive queries of one sequence, one kv head and 8 of its query heads.
-// The 128 MMA rows of a head tile are 4 query heads x 32 queries, row r = 4 * query + head,
-// exactly what one TMA box {64 dims, 4 heads, 32 tokens} of the [tokens][heads][dims] layout
-// delivers; two head tiles hold the 8 heads. With a window of at most 128 keys every row of
-// the unit sees only keys in the span [q0 - 128, q0 + 32) of its sequence, so per head tile one
-// S MMA of N = 160 covers the whole unit, one K tile and one V tile of 160 rows feed all 8
-// heads, and each softmax thread exponentiates 160 columns of its row. (The general kernel
-// tiles a window-128 call as 128 queries x 2 key tiles of 128 for 2 heads: two masked steps
-// per unit and 256 exponentials per row.)
+// The 128 MMA rows of a head tile are 8 query heads x 16 queries, row r = 8 * query + head,
+// exactly what one TMA box {64 dims, 8 heads, 16 tokens} of the [tokens][heads][dims] layout
+// delivers; head tile t holds queries q0 + 16 t .. q0 + 16 t + 15. With a window of at most 128
+// keys every row of the unit sees only keys in the span [q0 - 128, q0 + 32) of its sequence:
+// one K tile and one V tile of those 160 rows feed both head tiles, and head tile t needs its
+// rows 16 t .. 16 t + 143, so per head tile one S MMA of N = 144 covers the whole unit and each
+// softmax thread exponentiates 144 columns of its row. (The general kernel tiles a window-128
+// call as 128 queries x 2 key tiles of 128 for 2 heads: two masked steps per unit and 256
+// exponentials per row.)
 //
 // Per CTA (384 threads, one CTA per SM, persistent over a static list of units; all units
 // cost the same, so CTA c takes units c, c + grid, ...; consecutive CTAs take consecutive
@@ -18,15 +19,15 @@
 //   warp 0      TMA producer of Q (both head tiles) and K
 //   warp 2      TMA producer of V
 //   warps 1, 3  MMA issuers of head tile 0 / 1: PV_t(u-1) then S_t(u), since P_t is written
-//               over the first 80 columns of S_t (bf16 pairs)
+//               over the first 72 columns of S_t (bf16 pairs)
 //   warps 4-7   softmax of head tile 0, warps 8-11 of head tile 1; thread r owns row r
 //               (TMEM lane r). Per unit: the exact row maximum of the visible columns, the
 //               running maximum seeded with the head's sink (§Sink-Attention ¶3), P as bf16
 //               into TMEM, the sum d including the sink's term. A unit is one step, so there
-//               is no rescaling. The unit's epilogue (O / d as bf16, log-sum-exp) runs at the
-//               start of the warpgroup's next unit: S_t(u+1) is issued after PV_t(u) and MMAs
-//               complete in order, so O_t(u) is final by then and nothing waits for it.
-// TMEM (512 columns): head tile t has S_t (fp32, 160 columns) at 256 t, P_t (bf16 pairs, 80
+//               is no rescaling. The two warpgroups take turns (named barriers) from the TMEM
+//               load of S to the P store; the epilogue (O / d as bf16 through shared memory and
+//               one TMA store per head tile, log-sum-exp) follows PV_t(u) outside the turn.
+// TMEM (512 columns): head tile t has S_t (fp32, 144 columns) at 256 t, P_t (bf16 pairs, 72
 // columns) over the first half of S_t, and O_t (fp32, 64 columns) at 256 t + 160.
 // Every mbarrier wait is bounded; a timeout aborts the CTA cleanly through the same exits.
 #include <limits.h>
@@ -38,7 +39,9 @@ namespace sa {
 namespace {
 
 constexpr int kQB = 32;      // queries per unit
+constexpr int kQT = 16;      // queries per head tile (x 8 heads = 128 MMA rows)
 constexpr int kSpan = 160;   // keys per unit: [q0 - 128, q0 + 32)
+constexpr int kSN = 144;     // keys per head tile: span rows 16 t .. 16 t + 143
 constexpr int kD = 64;       // head_dim
 constexpr int kThreads = 384;
 constexpr uint32_t kRegsLow = 72;    // producers and issuers
@@ -59,7 +62,7 @@ __device__ __forceinline__ void turn_pass(uint32_t id) {
 }
 
 struct BandSmem {
-  static constexpr int kQTile = 128 * 128;     // one head tile of Q: 128 rows x 128 bytes
+  static constexpr int kQTile = 128 * 128;     // one head tile of Q (or O): 128 rows x 128 bytes
   static constexpr int kKVTile = kSpan * 128;  // one K or V span: 160 rows x 128 bytes
   static constexpr int kNQ = 2, kNK = 2, kNV = 2;
   static constexpr int kQ = 0;  // [kNQ][2 head tiles]
@@ -208,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (warp == 0 || warp == 2) {
       // ============ TMA producers: warp 0 loads Q and K, warp 2 loads V ============
-      // Per unit: Q of both head tiles (heads h, h+1, h+2, h+3 and h+4 .. h+7 of 32 queries)
-      // and the 160-row K span, or the V span. Rows before the first row or past the last
+      // Per unit: Q of both head tiles (heads h .. h+7 of queries q0 .. q0+15 and of q0+16 ..
+      // q0+31) and the 160-row K span, or the V span. Rows before the first row or past the last
       // one are filled with zeros by the copy; rows of a neighbouring sequence are masked.
       const bool qk = warp == 0;
       if (elect_one()) {
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(S::kBarQFull + qs), 2 * S::kQTile);
             for (int t = 0; t < 2; ++t)
               tma_load_3d(q_smem + (2 * qs + t) * S::kQTile, &tm_q, bar(S::kBarQFull + qs), 0,
-                          h0 + 4 * t, u.start + u.q0);
+                          h0, u.start + u.q0 + kQT * t);
           }
           __syncwarp();
           ++qc;
@@ -263,15 +266,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // ============ MMA issuers: warp 1 for head tile 0, warp 3 for head tile 1 ============
       // Per unit u: PV_t(u-1) (P_t(u-1) written, V resident, O_t read out by the epilogue of
-      // u-2), then S_t(u) = Q_t K^T (M = 128, N = 160, K = 64) into S_t.
+      // u-2), then S_t(u) = Q_t K^T (M = 128, N = 144, K = 64) into S_t, with K rows 16 t ..
+      // 16 t + 143 of the span (whole 1024-byte swizzle atoms from the tile's start).
       const int t = warp == 1 ? 0 : 1;
-      constexpr uint32_t idS = idesc_bf16_f32(128, kSpan, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, kSN, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, kD, false, true);
       constexpr uint32_t hi = sdesc_sw128_hi(1024);
       const uint32_t lo_q0 = sdesc_sw128_lo(q_smem, 16);
       const uint32_t lo_k0 = sdesc_sw128_lo(k_smem, 16);
       const uint32_t lo_v0 = sdesc_sw128_lo(v_smem, 16384);
-      const uint32_t dS = tmem + 256u * t, dO = dS + kSpan, aP = dS;
+      const uint32_t dS = tmem + 256u * t, dO = dS + 160, aP = dS;
+      const uint32_t span_off = (uint32_t)(kQT * 128 * t) >> 4;  // rows 16 t.. of K and V
       int qc = 0, kc = 0, vc = 0, n = 0;
       bool ok = true;
       auto do_pv = [&](int j) -> bool {  // PV_t of this tile's unit number j
@@ -280,10 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0 && !wait(bar(S::kBarOFree + t), (j - 1) & 1)) return false;
         if (!wait(bar(S::kBarPFull + t), j & 1)) return false;
         tc_fence_after_sync();
-        const uint32_t bv = lo_v0 + vs * (S::kKVTile >> 4);
+        const uint32_t bv = lo_v0 + vs * (S::kKVTile >> 4) + span_off;
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kSpan / 16; ++kk)  // 16 keys (2048 bytes of V) per MMA
+          for (int kk = 0; kk < kSN / 16; ++kk)  // 16 keys (2048 bytes of V) per MMA
             umma_ts(dO, aP + kk * 8, sdesc_join(bv + kk * (2048 >> 4), hi), idPV, kk > 0 ? 1u : 0u);
           umma_commit(bar(S::kBarODone + t));
           umma_commit(bar(S::kBarVEmpty + vs));
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait(bar(S::kBarKFull + ks), (kc / S::kNK) & 1))) break;
         tc_fence_after_sync();
         const uint32_t aq = lo_q0 + (2 * qs + t) * (S::kQTile >> 4);
-        const uint32_t bk = lo_k0 + ks * (S::kKVTile >> 4);
+        const uint32_t bk = lo_k0 + ks * (S::kKVTile >> 4) + span_off;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk)  // 32 bytes of each row per K = 16 step
@@ -336,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - 4) >> 2;  // head tile of this warpgroup
     const int quarter = warp & 3;   // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row = quarter * 32 + lane;
-    const int tok = row >> 2, hs = row & 3;  // row = 4 * query + head
+    const int tok = row >> 3, hs = row & 7;  // row = 8 * query + head
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + 256u * t;
-    const uint32_t ts = tl, tp = tl, to = tl + kSpan;
+    const uint32_t ts = tl, tp = tl, to = tl + 160;
     const float sl = p.scale_log2;
     const float2 sl2 = make_float2(sl, sl);
     // The two warpgroups take turns through named barriers: a turn runs from the TMEM load of
@@ -352,43 +357,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const BandUnit u = unit_at(i);
       if (u.len == 0) continue;
       stage = 0;
-      const int h = (u.go & 0xffff) * p.G + 8 * (u.go >> 16) + 4 * t + hs;
-      const int qi = u.q0 + tok;  // query position inside its sequence
+      const int h = (u.go & 0xffff) * p.G + 8 * (u.go >> 16) + hs;
+      const int qt = u.q0 + kQT * t;  // the head tile's first query inside its sequence
+      const int qi = qt + tok;        // this row's query
       const float m0 = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(S::kBarSFull + t), n & 1, wc)))) break;
       turn_wait(kNbTurn + t);  // the other warpgroup's turn is over
       stage = 1;
       tc_fence_after_sync();
-      uint32_t r[kSpan];
-      tmem_ld160(ts, r);
-      float s[kSpan];
+      uint32_t r[kSN];
+      tmem_ld144(ts, r);
+      float s[kSN];
 #pragma unroll
-      for (int c = 0; c < kSpan; ++c) s[c] = __uint_as_float(r[c]);
-      // Span column c holds key position q0 - 128 + c; visible: lo <= c <= hi (the key at or
-      // before the query, inside the window, and not before the sequence's first row).
+      for (int c = 0; c < kSN; ++c) s[c] = __uint_as_float(r[c]);
+      // Column c holds key position qt - 128 + c; visible: lo <= c <= hi (the key at or before
+      // the query, inside the window, and not before the sequence's first row).
       const int hi = tok + 128;
-      const int lo = max(128 - u.q0, tok + 129 - p.window);
-      // Columns 32..127 are visible to every row of the unit when the window is 128 keys and
-      // the span starts at or after the sequence's first row plus 32 (q0 >= 96): then only
-      // the first and the last 32 columns are masked.
-      const bool mid_visible = u.q0 >= 96 && p.window >= 128;
-      // One visibility word per 32 columns, then one bit test per column.
+      const int lo = max(128 - qt, tok + 129 - p.window);
+      // Columns 16..127 are visible to every row of the tile when the window is 128 keys and
+      // its keys start at or after the sequence's first row plus 16 (qt >= 112): then only the
+      // first and the last 16 columns are masked.
+      const bool mid_visible = qt >= 112 && p.window >= 128;
+      // One visibility word per 16 columns, then one bit test per column.
 #pragma unroll
-      for (int b = 0; b < kSpan / 32; ++b) {
-        if (b != 0 && b != kSpan / 32 - 1 && mid_visible) continue;
-        const int hc = min(max(hi, 32 * b - 1), 32 * b + 31) - 32 * b;  // -1 .. 31
-        const int lc = min(max(lo, 32 * b), 32 * b + 32) - 32 * b;      // 0 .. 32
+      for (int b = 0; b < kSN / 16; ++b) {
+        if (b != 0 && b != kSN / 16 - 1 && mid_visible) continue;
+        const int hc = min(max(hi, 16 * b - 1), 16 * b + 15) - 16 * b;  // -1 .. 15
+        const int lc = min(max(lo, 16 * b), 16 * b + 16) - 16 * b;      // 0 .. 16
         const uint32_t vis =
-            hc >= lc ? (0xffffffffu >> (31 - hc)) & (0xffffffffu << lc) : 0u;  // bits lc..hc
+            hc >= lc ? (0xffffu >> (15 - hc)) & (0xffffu << lc) : 0u;  // bits lc..hc
 #pragma unroll
-        for (int c = 0; c < 32; ++c) s[32 * b + c] = (vis & (1u << c)) ? s[32 * b + c] : -INFINITY;
+        for (int c = 0; c < 16; ++c) s[16 * b + c] = (vis & (1u << c)) ? s[16 * b + c] : -INFINITY;
       }
       // Row maximum of the visible columns: 8 independent three-input chains, then 8 -> 1.
       float mp[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) mp[a] = fmaxf(s[a], s[8 + a]);
 #pragma unroll
-      for (int c = 16; c < kSpan; c += 16) {
+      for (int c = 16; c < kSN; c += 16) {
 #pragma unroll
         for (int a = 0; a < 8; ++a) mp[a] = fmax3(mp[a], s[c + a], s[c + 8 + a]);
       }
@@ -399,8 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 nmu = make_float2(-mu, -mu);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};  // independent partial row sums
+      // P over S_t's columns, all of which are already in registers: four blocks of 32
+      // columns (16 packed words) and one of 16.
 #pragma unroll
-      for (int c4 = 0; c4 < kSpan / 32; ++c4) {
+      for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -410,7 +418,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[e & 3] = fadd2(acc[e & 3], pe);
           pk[e] = pack_bf16x2(pe.x, pe.y);
         }
-        tmem_st16(tp + 16 * c4, pk);  // P over S_t's columns already read into registers
+        tmem_st16(tp + 16 * c4, pk);
+      }
+      {
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = 128 + 2 * e;
+          const float2 x = ffma2(make_float2(s[c], s[c + 1]), sl2, nmu);
+          const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+          acc[e & 3] = fadd2(acc[e & 3], pe);
+          pk[e] = pack_bf16x2(pe.x, pe.y);
+        }
+        tmem_st8(tp + 64, pk);
       }
       turn_pass(kNbTurn + (t ^ 1));
       stage = 2;
@@ -425,24 +445,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = d > 0.f ? 1.f / d : 0.f;
       const bool row_ok = qi < u.len;
       const size_t orow = (size_t)(u.start + qi) * p.Hq + h;
-      if (u.len - u.q0 >= kQB) {
-        // A whole block of 32 queries: the rows go to shared memory in the layout of the
-        // output box (row = 4 * query + head, 128-byte swizzle) and leave in one TMA store per
-        // head tile, instead of 128 threads storing 128 bytes each.
+      if (u.len - qt >= kQT) {
+        // All 16 queries of the tile in the sequence: the rows go to shared memory in the
+        // layout of the output box (row = 8 * query + head, 128-byte swizzle) and leave in one
+        // TMA store, instead of 128 threads storing 128 bytes each.
         const uint32_t obuf = o_smem + t * S::kQTile;
         if (row == 0) bulk_wait_group_read0();  // this tile's previous store has read obuf
         named_barrier_sync(kNbEpi + t, 128);
+        uint32_t o[kD];
+        tmem_ld64(to, o);
 #pragma unroll
         for (int c4 = 0; c4 < kD / 32; ++c4) {
-          uint32_t o[32];
-          tmem_ld32(to + 32 * c4, o);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint32_t w4[4];
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2)
-              w4[k2] = pack_bf16x2(__uint_as_float(o[8 * e + 2 * k2]) * inv,
-                                   __uint_as_float(o[8 * e + 2 * k2 + 1]) * inv);
+              w4[k2] = pack_bf16x2(__uint_as_float(o[32 * c4 + 8 * e + 2 * k2]) * inv,
+                                   __uint_as_float(o[32 * c4 + 8 * e + 2 * k2 + 1]) * inv);
             const int chunk = 4 * c4 + e;  // 16-byte chunk of the 128-byte row
             const uint32_t a = obuf + row * 128 + ((chunk ^ (row & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w4[0]),
@@ -453,12 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         named_barrier_sync(kNbEpi + t, 128);
         if (row == 0) {
-          tma_store_3d(&tm_o, obuf, 0, (u.go & 0xffff) * p.G + 8 * (u.go >> 16) + 4 * t,
-                       u.start + u.q0);
+          tma_store_3d(&tm_o, obuf, 0, (u.go & 0xffff) * p.G + 8 * (u.go >> 16), u.start + qt);
           bulk_commit_group();
         }
       } else {
-        // The sequence's last, partial block: per-row stores, rows of this sequence only.
+        // A tile past the sequence's last row: per-row stores, rows of this sequence only.
         uint4* dst = reinterpret_cast<uint4*>(p.out + (row_ok ? orow : 0) * kD);
 #pragma unroll
         for (int c4 = 0; c4 < kD / 32; ++c4) {
@@ -498,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e.y == 0) continue;
         if (stage < 1) turn_wait(kNbTurn + t);
         if (stage < 2) turn_pass(kNbTurn + (t ^ 1));
-        if (e.y - e.z >= kQB) {
+        if (e.y - (e.z + kQT * t) >= kQT) {
           named_barrier_sync(kNbEpi + t, 128);
           named_barrier_sync(kNbEpi + t, 128);
         }

@@ -354,9 +354,9 @@ __device__ __forceinline__ float tmem_ld128_max(uint32_t taddr, uint32_t (&r)[12
   return fmaxf(m0, m1);
 }
 
-// 160 consecutive fp32 columns of this thread's TMEM lane (an x128 and an x32 load, one
+// 144 consecutive fp32 columns of this thread's TMEM lane (an x128 and an x16 load, one
 // wait).
-__device__ __forceinline__ void tmem_ld160(uint32_t taddr, uint32_t (&r)[160]) {
+__device__ __forceinline__ void tmem_ld144(uint32_t taddr, uint32_t (&r)[144]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -366,16 +366,37 @@ __device__ __forceinline__ void tmem_ld160(uint32_t taddr, uint32_t (&r)[160]) {
       "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
       "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
       "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
-      "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%160];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%128, %129, %130, %131, %132, %133, %134, %135, %136, %137, %138, %139, %140, %141, %142, %143, "
-      "%144, %145, %146, %147, %148, %149, %150, %151, %152, %153, %154, %155, %156, %157, %158, %159}, [%161];\n\t"
+      "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%144];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%128, %129, %130, %131, %132, %133, %134, %135, %136, %137, %138, %139, %140, %141, %142, %143}, [%145];\n\t"
       "tcgen05.wait::ld.sync.aligned;\n"
       : SA_R8(0), SA_R8(8), SA_R8(16), SA_R8(24), SA_R8(32), SA_R8(40), SA_R8(48), SA_R8(56),
         SA_R8(64), SA_R8(72), SA_R8(80), SA_R8(88), SA_R8(96), SA_R8(104), SA_R8(112), SA_R8(120),
-        SA_R8(128), SA_R8(136), SA_R8(144), SA_R8(152)
+        SA_R8(128), SA_R8(136)
       : "r"(taddr), "r"(taddr + 128)
       : "memory");
+}
+
+// 64 consecutive fp32 columns of this thread's TMEM lane (one x64 load and its wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : SA_R8(0), SA_R8(8), SA_R8(16), SA_R8(24), SA_R8(32), SA_R8(40), SA_R8(48), SA_R8(56)
+      : "r"(taddr)
+      : "memory");
+}
+
+// Store 8 consecutive 32-bit columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                   taddr),
+               SA_W8(0)
+               : "memory");
 }
 
 // Store 16 consecutive 32-bit columns of this thread's TMEM lane (no wait).
