@@ -26,7 +26,7 @@ struct PrefillLaunch {
   uint64_t timeout_ns;
   int band;                      // the short-window kernel: tm_q has box {64, 8, 16} and
                                  // tm_k/tm_v box {64, 1, 160} (prefill_band_applies)
-  CUtensorMap tm_o;              // band: `out` as {head_dim, heads, tokens}, box {64, 8, 16}
+  CUtensorMap tm_o;              // band: `out` as {head_dim, heads, tokens}, box {64, 8, 4}
 };
 
 // The short-window prefill kernel (prefill_band.cu): 32 queries x 8 query heads per unit

@@ -25,8 +25,10 @@
 //               running maximum seeded with the head's sink (§Sink-Attention ¶3), P as bf16
 //               into TMEM, the sum d including the sink's term. A unit is one step, so there
 //               is no rescaling. The two warpgroups take turns (named barriers) from the TMEM
-//               load of S to the P store; the epilogue (O / d as bf16 through shared memory and
-//               one TMA store per head tile, log-sum-exp) follows PV_t(u) outside the turn.
+//               load of S to the P store; the epilogue (O / d as bf16, log-sum-exp) follows
+//               PV_t(u) outside the turn.
+// Output: each softmax warp stages its 32 rows (4 queries x 8 heads) in shared memory and
+// writes them with one TMA store (box {64, 8, 4}), or with per-row stores past a sequence's end.
 // TMEM (512 columns): head tile t has S_t (fp32, 144 columns) at 256 t, P_t (bf16 pairs, 72
 // columns) over the first half of S_t, and O_t (fp32, 64 columns) at 256 t + 160.
 // Every mbarrier wait is bounded; a timeout aborts the CTA cleanly through the same exits.
@@ -49,7 +51,6 @@ constexpr uint32_t kRegsHigh = 216;  // softmax warpgroups
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kNbTeardown = 1;
 constexpr uint32_t kNbTurn = 2;  // + t: softmax warpgroup t may take its turn (256 threads)
-constexpr uint32_t kNbEpi = 4;   // + t: the 128 threads of softmax warpgroup t (output staging)
 
 // Turn hand-overs between the two softmax warpgroups carry no data (each touches only its own
 // TMEM columns), so these forms do not clobber memory; being volatile they stay in order with
@@ -73,7 +74,8 @@ struct BandSmem {
   static constexpr int kBarQFull = 0, kBarQEmpty = kBarQFull + kNQ, kBarKFull = kBarQEmpty + kNQ,
                        kBarKEmpty = kBarKFull + kNK, kBarVFull = kBarKEmpty + kNK,
                        kBarVEmpty = kBarVFull + kNV, kBarSFull = kBarVEmpty + kNV,  // [2]
-      kBarPFull = kBarSFull + 2, kBarODone = kBarPFull + 2, kBarOFree = kBarODone + 2,
+      kBarPFull = kBarSFull + 2,  // [2] P of keys 0..95 written, [2] P of keys 96..143 written
+      kBarODone = kBarPFull + 4, kBarOFree = kBarODone + 2,
                        kBarDrain = kBarOFree + 2, kNumBars = kBarDrain + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;  // [0] tmem base, [1] abort flag
   static constexpr int kPre = kMisc + 16;            // int [kBandMaxSeqs + 1]: query blocks
@@ -128,8 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < S::kNumBars; ++i) {
       // Q, K and V stages are released by both issuers (one commit each); P written and O
       // read out are arrivals of the 128 softmax threads of a head tile.
-      const bool by_threads = (i == S::kBarPFull || i == S::kBarPFull + 1 ||
-                               i == S::kBarOFree || i == S::kBarOFree + 1);
+      const bool by_threads = (i >= S::kBarPFull && i < S::kBarPFull + 4) ||
+                              i == S::kBarOFree || i == S::kBarOFree + 1;
       const bool by_issuers = (i >= S::kBarQEmpty && i < S::kBarQEmpty + S::kNQ) ||
                               (i >= S::kBarKEmpty && i < S::kBarKEmpty + S::kNK) ||
                               (i >= S::kBarVEmpty && i < S::kBarVEmpty + S::kNV);
@@ -283,13 +285,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vs = vc % S::kNV;
         if (!wait(bar(S::kBarVFull + vs), (vc / S::kNV) & 1)) return false;
         if (j > 0 && !wait(bar(S::kBarOFree + t), (j - 1) & 1)) return false;
+        // P arrives in two parts (keys 0..95, then 96..143), so the first six MMAs run while
+        // the softmax still computes the last 48 columns.
         if (!wait(bar(S::kBarPFull + t), j & 1)) return false;
         tc_fence_after_sync();
         const uint32_t bv = lo_v0 + vs * (S::kKVTile >> 4) + span_off;
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kSN / 16; ++kk)  // 16 keys (2048 bytes of V) per MMA
+          for (int kk = 0; kk < 6; ++kk)  // 16 keys (2048 bytes of V) per MMA
             umma_ts(dO, aP + kk * 8, sdesc_join(bv + kk * (2048 >> 4), hi), idPV, kk > 0 ? 1u : 0u);
+        }
+        __syncwarp();
+        if (!wait(bar(S::kBarPFull + 2 + t), j & 1)) return false;
+        tc_fence_after_sync();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 6; kk < kSN / 16; ++kk)
+            umma_ts(dO, aP + kk * 8, sdesc_join(bv + kk * (2048 >> 4), hi), idPV, 1u);
           umma_commit(bar(S::kBarODone + t));
           umma_commit(bar(S::kBarVEmpty + vs));
         }
@@ -419,6 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[e] = pack_bf16x2(pe.x, pe.y);
         }
         tmem_st16(tp + 16 * c4, pk);
+        if (c4 == 2) {  // keys 0..95 written: the first six PV MMAs may start
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(bar(S::kBarPFull + t));
+        }
       }
       {
         uint32_t pk[8];
@@ -438,20 +455,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float d = ex2(m0 - mu) + ((a01.x + a23.x) + (a01.y + a23.y));  // the sink's term
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(bar(S::kBarPFull + t));
+      mbar_arrive(bar(S::kBarPFull + 2 + t));
       // ---- epilogue: O / d -> bf16 once PV_t(u) is done, rows of this sequence only ----
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(S::kBarODone + t), n & 1, wc)))) break;
       tc_fence_after_sync();
       const float inv = d > 0.f ? 1.f / d : 0.f;
       const bool row_ok = qi < u.len;
       const size_t orow = (size_t)(u.start + qi) * p.Hq + h;
-      if (u.len - qt >= kQT) {
-        // All 16 queries of the tile in the sequence: the rows go to shared memory in the
-        // layout of the output box (row = 8 * query + head, 128-byte swizzle) and leave in one
-        // TMA store, instead of 128 threads storing 128 bytes each.
-        const uint32_t obuf = o_smem + t * S::kQTile;
-        if (row == 0) bulk_wait_group_read0();  // this tile's previous store has read obuf
-        named_barrier_sync(kNbEpi + t, 128);
+      if (u.len - (qt + 4 * quarter) >= 4) {
+        // The warp's 4 queries (x 8 heads) all in the sequence: its 32 rows go to its 4 KB of
+        // shared memory in the layout of the output box (row = 8 * query + head, 128-byte
+        // swizzle) and leave in one TMA store of the warp, instead of 32 stores of 128 bytes.
+        const uint32_t wbuf = o_smem + t * S::kQTile + quarter * 4096;
+        if (lane == 0) bulk_wait_group_read0();  // the warp's previous store has read wbuf
+        __syncwarp();
         uint32_t o[kD];
         tmem_ld64(to, o);
 #pragma unroll
@@ -464,20 +481,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               w4[k2] = pack_bf16x2(__uint_as_float(o[32 * c4 + 8 * e + 2 * k2]) * inv,
                                    __uint_as_float(o[32 * c4 + 8 * e + 2 * k2 + 1]) * inv);
             const int chunk = 4 * c4 + e;  // 16-byte chunk of the 128-byte row
-            const uint32_t a = obuf + row * 128 + ((chunk ^ (row & 7)) << 4);
+            const uint32_t a = wbuf + lane * 128 + ((chunk ^ (lane & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w4[0]),
                          "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
                          : "memory");
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        named_barrier_sync(kNbEpi + t, 128);
-        if (row == 0) {
-          tma_store_3d(&tm_o, obuf, 0, (u.go & 0xffff) * p.G + 8 * (u.go >> 16), u.start + qt);
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, wbuf, 0, (u.go & 0xffff) * p.G + 8 * (u.go >> 16),
+                       u.start + qt + 4 * quarter);
           bulk_commit_group();
         }
       } else {
-        // A tile past the sequence's last row: per-row stores, rows of this sequence only.
+        // Queries past the sequence's last row: per-row stores, rows of this sequence only.
         uint4* dst = reinterpret_cast<uint4*>(p.out + (row_ok ? orow : 0) * kD);
 #pragma unroll
         for (int c4 = 0; c4 < kD / 32; ++c4) {
@@ -510,22 +528,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Dry tail: the remaining turn hand-overs of this warpgroup's list, all blocking, so
       // that the partner warpgroup (which aborts as well, its waits seeing the abort flag)
       // never waits on a turn that does not come.
-      // The output staging barriers of whole blocks are met the same way (a warp aborts only
-      // in a wait before its turn or before its epilogue).
       for (; i < n_list; ++i, stage = 0) {
-        const int4 e = list[i];
-        if (e.y == 0) continue;
+        if (list[i].y == 0) continue;
         if (stage < 1) turn_wait(kNbTurn + t);
         if (stage < 2) turn_pass(kNbTurn + (t ^ 1));
-        if (e.y - (e.z + kQT * t) >= kQT) {
-          named_barrier_sync(kNbEpi + t, 128);
-          named_barrier_sync(kNbEpi + t, 128);
-        }
       }
     }
     // Warpgroup 1's hand-overs lead warpgroup 0's turns by one: take the last.
     if (t == 0) turn_wait(kNbTurn + 0);
-    if (row == 0) bulk_wait_group0();  // this tile's output stores are complete
+    if (lane == 0) bulk_wait_group0();  // the warp's output stores are complete
     __syncwarp();
     tc_fence_before_sync();
     named_barrier_sync(kNbTeardown, kThreads);

@@ -215,7 +215,7 @@ sink_attn_status prefill_impl(const sink_attn_bf16* q, const sink_attn_bf16* k,
                : 0;
   const bool maps_ok =
       a.band ? encode_3d(&a.tm_q, q, head_dim, num_q_heads, total_tokens, 16, 8) &&
-                   encode_3d(&a.tm_o, out, head_dim, num_q_heads, total_tokens, 16, 8) &&
+                   encode_3d(&a.tm_o, out, head_dim, num_q_heads, total_tokens, 4, 8) &&
                    encode_3d(&a.tm_k, k, head_dim, num_kv_heads, rows_k, 160) &&
                    encode_3d(&a.tm_v, v, head_dim, num_kv_heads, rows_k, 160)
              : encode_3d(&a.tm_q, q, head_dim, num_q_heads, total_tokens, 128) &&
