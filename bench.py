@@ -51,8 +51,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by the SHA-256 of the kernel source it was taken on; stale entries are ignored.
 NCU_TRAFFIC = {
-    # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 194.8 MB read + 117.0 MB written
-    "prefill_tc.cu:c64132d724481f28": 311.8e6,
+    # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 195.5 MB read + 116.5 MB written
+    "prefill_tc.cu:1a4ec468a4219454": 312.1e6,
+    # prefill_band_kernel, gpt-oss window 128: 193.3 MB read + 108.8 MB written
+    "prefill_band.cu:ec5a763b7ab861de": 302.1e6,
     # decode_split_kernel<64,1,false,8>, gpt-oss decode: 691.5 MB read + 7.3 MB written
     "decode_split.cu:fead54c850f5b7b4": 698.8e6,
 }
@@ -490,10 +492,12 @@ def run_ours(args):
                      "peak_source": f"bf16_tflops burst, {peak_src}"},
         "prefill_window128": {"value": round(tflops_w, 3), "unit": "TFLOP/s",
                               "frac": round(tflops_w / peak_tc, 4),
+                              "kernel": "prefill_band_kernel (32 queries x 8 heads per unit)",
                               "hbm": {"algorithmic_bytes": pw_bytes,
                                       "achieved_gbs": round(pw_bytes / (mean["prefill_w128"] * 1e-3) / 1e9, 1),
                                       "frac": round(pw_bytes / (mean["prefill_w128"] * 1e-3) / 1e9
-                                                    / peak_hbm, 4)},
+                                                    / peak_hbm, 4),
+                                      "traffic": traffic("prefill_band.cu")},
                               "note": "about 4e10 flop against 346 MB of Q, K, V and output: "
                                       "the HBM time of its bytes (51 us) is the floor"},
         "decode": {"value": round(job_rate(db, ws, mean["decode"]) / 1e9, 2), "unit": "GB/s",
