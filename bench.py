@@ -56,7 +56,7 @@ NCU_TRAFFIC = {
     # prefill_band_kernel, gpt-oss window 128: 193.3 MB read + 108.8 MB written
     "prefill_band.cu:ec5a763b7ab861de": 302.1e6,
     # decode_split_kernel<64,1,false,8>, gpt-oss decode: 691.5 MB read + 7.3 MB written
-    "decode_split.cu:fead54c850f5b7b4": 698.8e6,
+    "decode_split.cu:25b6e31ebae3f2fc": 698.8e6,
 }
 
 
