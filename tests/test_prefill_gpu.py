@@ -260,6 +260,9 @@ LONG = {
                                                                       seed=77),
     "one 32768-token sequence D128 G16 W128": lambda: wl.prefill_case([32768], 64, 4, 128,
                                                                       window=128, seed=78),
+    # the short-window kernel over 1024 query blocks of one sequence
+    "one 32768-token sequence D64 G8 W128": lambda: wl.prefill_case([32768], 64, 8, 64,
+                                                                    window=128, seed=79),
 }
 
 
@@ -282,16 +285,18 @@ def test_prefill_long_sequence_sampled(name):
     assert_clean_device()
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_nan_input_row_stays_local(d):
+@pytest.mark.parametrize("d,window", [(64, 0), (128, 0), (64, 128)])
+def test_nan_input_row_stays_local(d, window):
     """A NaN in one query row makes that row's output NaN and nothing else. The row's
     softmax state (max and sum) is NaN in only some lanes of a warp, so any warp-aligned
-    step that takes a per-lane value as its condition would diverge here."""
-    case = wl.prefill_case([300, 129], 16, 2, d, seed=900 + d)
+    step that takes a per-lane value as its condition would diverge here. Window 128 with
+    groups of 8 runs the short-window kernel."""
+    case = wl.prefill_case([300, 129], 16, 2, d, window=window, seed=900 + d)
     q = case.q.clone()
     q[7, 3, 5] = float("nan")
     got = sa.sink_attn_prefill(q.cuda(), case.k.cuda(), case.v.cuda(), case.sinks.cuda(),
-                               case.cu_seqlens.cuda(), case.max_seqlen, scale=case.scale)
+                               case.cu_seqlens.cuda(), case.max_seqlen, window=window,
+                               scale=case.scale)
     got = got.float().cpu()
     assert torch.isnan(got[7, 3]).all()
     rest = torch.ones(got.shape[:2], dtype=torch.bool)
@@ -299,7 +304,7 @@ def test_nan_input_row_stays_local(d):
     assert torch.isfinite(got[rest]).all()
     ref = ref_prefill(case)
     got[7, 3] = torch.from_numpy(ref[7, 3]).float()  # the NaN row was checked above
-    assert_parity(got, ref, f"NaN query row D{d}")
+    assert_parity(got, ref, f"NaN query row D{d} W{window}")
     assert_clean_device()
 
 
