@@ -175,8 +175,10 @@ def test_prefill_empty_inputs_are_noops():
     assert_clean_device()
 
 
-def test_prefill_bad_cu_seqlens_reported_not_faulted():
-    case = wl.prefill_case([64, 64], 4, 2, 64, seed=13)
+@pytest.mark.parametrize("hq,hkv,window", [(4, 2, 0), (8, 1, 128)])
+def test_prefill_bad_cu_seqlens_reported_not_faulted(hq, hkv, window):
+    """(8, 1, 128) runs the short-window kernel."""
+    case = wl.prefill_case([64, 64], hq, hkv, 64, window=window, seed=13)
     bad = torch.tensor([0, 64, 1000], dtype=torch.int32)  # past total_tokens
     out = torch.zeros_like(case.q.cuda())
     gpu_prefill(case, out=out, cu=bad)
@@ -187,8 +189,9 @@ def test_prefill_bad_cu_seqlens_reported_not_faulted():
     assert_parity(out[:64], ref[:64], "first sequence")
 
 
-def test_prefill_max_seqlen_too_small_reported():
-    case = wl.prefill_case([300], 4, 2, 64, seed=14)
+@pytest.mark.parametrize("hq,hkv,window", [(4, 2, 0), (8, 1, 128)])
+def test_prefill_max_seqlen_too_small_reported(hq, hkv, window):
+    case = wl.prefill_case([300], hq, hkv, 64, window=window, seed=14)
     gpu_prefill(case, max_seqlen=128)
     st, b = sa.sink_attn_read_device_error()
     assert st == 5 and (b & 0x2)
