@@ -32,8 +32,6 @@
 // TMEM (512 columns): head tile t has S_t (fp32, 144 columns) at 256 t, P_t (bf16 pairs, 72
 // columns) over the first half of S_t, and O_t (fp32, 64 columns) at 256 t + 160.
 // Every mbarrier wait is bounded; a timeout aborts the CTA cleanly through the same exits.
-#include <limits.h>
-
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 

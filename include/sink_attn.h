@@ -130,7 +130,8 @@ typedef enum sink_attn_status {
  *              [cu_seqlens[s], cu_seqlens[s+1]) of q, k, v and out.
  *   max_seqlen host-side upper bound of every sequence length (>= 0). A longer
  *              sequence sets SINK_ATTN_DEVERR_CU_SEQLENS; its rows past the bound
- *              are not written.
+ *              hold unspecified values afterwards (a kernel may or may not write
+ *              them).
  *   window     W > 0: sliding window of W keys; W <= 0: full causal.
  *   scale      multiplier of q·k (typically 1/sqrt(head_dim)).
  *   out        [total_tokens][num_q_heads][head_dim] bf16. Rows of tokens that
