@@ -93,6 +93,14 @@ CASES = {
     "band 300 sequences D64 G8 W64": lambda: wl.prefill_case(
         [int(x) for x in np.random.default_rng(26).integers(0, 200, 300)], 8, 1, 64, window=64,
         seed=26),
+    # the last window the short-window kernel takes, and the first it leaves to the general one
+    "band D64 G8 W127": lambda: wl.prefill_case([300, 129, 1], 8, 1, 64, window=127, seed=27),
+    "D64 G8 W129 (general kernel)": lambda: wl.prefill_case([300, 129, 1], 8, 1, 64, window=129,
+                                                            seed=28),
+    # as many sequences as the short-window kernel's sequence table holds
+    "band 1024 sequences D64 G8 W128": lambda: wl.prefill_case(
+        [int(x) for x in np.random.default_rng(29).integers(0, 40, 1024)], 8, 1, 64, window=128,
+        seed=29),
 }
 
 
