@@ -53,8 +53,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # prefill_kernel<64,0,0,0,1>, gpt-oss causal: 195.5 MB read + 116.5 MB written
     "prefill_tc.cu:1a4ec468a4219454": 312.1e6,
-    # prefill_band_kernel, gpt-oss window 128: 193.2 MB read + 108.1 MB written
-    "prefill_band.cu:5e62ecfdac8679d5": 301.3e6,
+    # prefill_band_kernel, gpt-oss window 128: 193.2 MB read + 108.6 MB written
+    "prefill_band.cu:64112c8817f75910": 301.8e6,
     # decode_split_kernel<64,1,false,8>, gpt-oss decode: 691.5 MB read + 7.3 MB written
     "decode_split.cu:25b6e31ebae3f2fc": 698.8e6,
 }

@@ -1,6 +1,8 @@
 // prefill_band.cu — sliding-window prefill for short windows (1..128 keys) at head_dim 64,
-// when each kv head serves a multiple of 8 query heads (gpt-oss: 64 query / 8 kv heads,
-// every other layer attending to a 128-token window; "GPT-OSS am Day 0", §Sink-Attention).
+// when each kv head serves a multiple of 8 query heads (the gpt-oss shape, 64 query / 8 kv
+// heads, with a 128-token window). The sink softmax is that of "GPT-OSS am Day 0",
+// §Sink-Attention; the pages do not describe windows, whose convention here is W keys, the
+// query's own included.
 //
 // Work unit: 32 consecutive queries of one sequence, one kv head and 8 of its query heads.
 // The 128 MMA rows of a head tile are 8 query heads x 16 queries, row r = 8 * query + head,
